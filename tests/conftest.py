@@ -1,0 +1,31 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
+    config.addinivalue_line("markers", "slow: long-running case")
+
+
+def read_golden(name):
+    """Parse a golden fixture: '#' comments, then 'key v1 v2 ...' or bare numeric rows."""
+    keyed, rows = {}, []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            try:
+                rows.append([float(p) for p in parts])
+            except ValueError:
+                keyed[parts[0]] = [float(p) for p in parts[1:]]
+    return keyed, rows
