@@ -1,0 +1,357 @@
+"""Benchmark of the Mixtral sparse-MoE feed-forward layer on B300.
+
+One "step" = one MoE layer call (router + top-2 gate, dispatch, W1/W3 grouped
+GEMM with fused SwiGLU, W2 grouped GEMM with gate scaling, combine) on one
+batch of synthetic Mixtral-shaped input (d=4096, d_ff=14336, 8 experts, top-2,
+seeded random weights; no checkpoint).  The headline workload is prefill with
+T=4096 tokens; the decode regime (T=32) is measured in the same run and
+reported as microseconds per layer.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torch.distributed.run: every rank runs an independent
+replica on its own GPU with its own batch (the layer is per-token independent:
+data parallel over tokens, no collective on the data path); the barrier and
+the max over ranks are for timing only.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the layer there is) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (T=4096 prefill) & µs/layer decode T=32; % of BF16/HBM roofline"
+
+
+def peaks():
+    p = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in m})
+        p["source"] = "measured"
+    return p
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return rank, ws, dist
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return 0, 1, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(v: float, dist) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+def algorithmic(T: int, counts, d=4096, F=14336, n=8, k=2):
+    """FLOPs and bytes of one layer call that the method itself requires."""
+    flops_router = 2.0 * T * d * n
+    flops_w13 = 4.0 * k * T * d * F
+    flops_w2 = 2.0 * k * T * d * F
+    touched = sum(1 for c in counts if c > 0)
+    w_bytes = touched * 3.0 * d * F * 2
+    act_bytes = 2.0 * T * d * 2 + n * d * 4
+    return dict(flops=flops_router + flops_w13 + flops_w2, flops_w13=flops_w13, flops_w2=flops_w2,
+                bytes=w_bytes + act_bytes, weight_bytes=w_bytes, touched=touched)
+
+
+def run_ours(args, rank, world, dist):
+    from sparse_mixture_experts_54_b300 import _lib, inputs
+    from sparse_mixture_experts_54_b300.layer import MoELayer
+
+    pk = peaks()
+    wp = inputs.workload("prefill_t4096")
+    wd = inputs.workload("decode_t32")
+    # every rank draws its own batch (data parallel over tokens); experts are the same model
+    W1, W3, W2 = inputs.make_experts(wp, "cuda")
+    xp = inputs.make_x(wp, "cuda", seed=rank)
+    xd = inputs.make_x(wd, "cuda", seed=rank)
+    Wg, _ = inputs.make_router(wp, "cuda")
+    m = MoELayer(wp.d, wp.d_ff, wp.n_experts, wp.k)
+    m.reserve(wp.T)
+    stream = torch.cuda.current_stream()
+
+    def timed(x, steps, warmup, stage_timing):
+        for _ in range(warmup):
+            m.forward(x, Wg, W1, W3, W2)
+        torch.cuda.synchronize()
+        m.set_option(_lib.MOE_OPT_STAGE_TIMING, 1 if stage_timing else 0)
+        m.stage_times()   # drop warm-up records
+        y = torch.empty((x.shape[0], wp.d), dtype=torch.bfloat16, device="cuda")
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            m.forward(x, Wg, W1, W3, W2, y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        ms = e0.elapsed_time(e1) / steps
+        stages, calls = m.stage_times()
+        m.set_option(_lib.MOE_OPT_STAGE_TIMING, 0)
+        assert m.status() == 0, _lib.moe_error_string(m.status())
+        return max_over_ranks(ms, dist), stages
+
+    # routing statistics of the prefill batch (for the algorithmic byte count)
+    r = m.route(xp, Wg)
+    counts_p = r["counts"].cpu().tolist()
+    r = m.route(xd, Wg)
+    counts_d = r["counts"].cpu().tolist()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms_p, stages_p = timed(xp, args.steps, args.warmup, True)
+        ms_d, stages_d = timed(xd, max(args.steps, 10), args.warmup, True)
+    clocks = clk.summary()
+
+    # end to end: pinned host x in, host y out, through the host-buffer entry point
+    xh = xp.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(args.warmup):
+        m.forward_host(xh, Wg, W1, W3, W2, yh)
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        m.forward_host(xh, Wg, W1, W3, W2, yh)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)
+
+    alg_p = algorithmic(wp.T, counts_p)
+    alg_d = algorithmic(wd.T, counts_d)
+    tok_s = world * wp.T / (ms_p * 1e-3)
+    # dominant kernel: the W1/W3 grouped GEMM (2/3 of the FLOPs)
+    k13_ms = stages_p.get("expert_w1w3_swiglu", float("nan"))
+    achieved = alg_p["flops_w13"] / (k13_ms * 1e-3) / 1e12
+    roofline = {"kernel": "expert_w1w3_swiglu (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
+                "achieved": round(achieved, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
+                "peak_kind": f"bf16 sustained ({pk['source']})",
+                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4),
+                "traffic": None}
+    layer_tflops = alg_p["flops"] / (ms_p * 1e-3) / 1e12
+    dec_gbs = alg_d["bytes"] / (ms_d * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_p, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0, 1/sqrt(fan_in)) weights, unit-RMS x)",
+        "config": {"workload": "prefill_t4096", "T": wp.T, "d": wp.d, "d_ff": wp.d_ff, "n_experts": wp.n_experts,
+                   "k": wp.k, "parallelism": f"replicas x{world} (data parallel over tokens)",
+                   "l2": "inputs larger than L2: 2.82 GB of expert weights streamed per step"},
+        "layer": {"us_per_layer": round(ms_p * 1e3, 1), "tflops": round(layer_tflops, 1),
+                  "frac_of_bf16_sustained": round(layer_tflops / pk["bf16_tflops_sustained"], 4),
+                  "frac_of_bf16_nominal_2250": round(layer_tflops / 2250.0, 4), "expert_loads": counts_p},
+        "decode_t32": {"us_per_layer": round(ms_d * 1e3, 1), "weight_gbytes": round(alg_d["weight_bytes"] / 1e9, 3),
+                       "experts_touched": alg_d["touched"], "achieved_gbs": round(dec_gbs, 1),
+                       "frac_of_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
+                       "frac_of_hbm_nominal_8000": round(dec_gbs / 8000.0, 4),
+                       "stages_us": {k: round(v * 1e3, 1) for k, v in stages_d.items()}},
+        "stages_us": {k: round(v * 1e3, 1) for k, v in stages_p.items()},
+        "roofline": roofline,
+        "e2e": {"value": round(world * wp.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+                "d2h_bytes_per_step": int(yh.numel() * yh.element_size()),
+                "ms_per_step": round(ms_e2e, 4), "entry_point": "moe_forward_host"},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clocks,
+    }
+    m.close()
+    host = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = dict(x=xp.cpu(), Wg=Wg.cpu(), W=(W1.cpu(), W3.cpu(), W2.cpu()))
+    return line, host
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def time_oracle(x, Wg, W, budget_s: float, min_tokens: int, seed: int = 0):
+    """Time the fp64 oracle on a bounded, seeded sample of the batch's tokens."""
+    import numpy as np
+
+    import oracle
+    from sparse_mixture_experts_54_b300 import inputs
+
+    xo = inputs.to_oracle(x)
+    Wgo = inputs.to_oracle(Wg)
+    W1, W3, W2 = (inputs.to_oracle(t) for t in W)
+    threads = oracle.max_threads()
+    T = xo.shape[0]
+    order = inputs.sample_tokens(T, T, seed).numpy()
+    rng = np.random.default_rng(seed)
+    rng.shuffle(order)
+    done, t_total = 0, 0.0
+    batch = max(threads, 1)
+    while done < T:
+        toks = np.sort(order[done:done + batch])
+        t0 = time.perf_counter()
+        oracle.moe_forward(xo[toks], Wgo, W1, W3, W2, 2, nthreads=threads)
+        t_total += time.perf_counter() - t0
+        done += len(toks)
+        if t_total >= budget_s and done >= min_tokens:
+            break
+    return dict(tokens=done, seconds=t_total, threads=threads, tok_s=done / t_total)
+
+
+def cpu_baseline_block(res, T):
+    return {"value": round(res["tok_s"], 3), "unit": "tokens/s", "cores": res["threads"], "kind": "oracle",
+            "sample": f"{res['tokens']} of the {T} prefill tokens (seeded sample), full routing + 2 SwiGLU experts "
+                      f"each in fp64, {res['seconds']:.1f} s on {res['threads']} host threads"}
+
+
+def run_reference(args, rank, world):
+    from sparse_mixture_experts_54_b300 import inputs
+
+    if rank != 0:
+        return None
+    w = inputs.workload("prefill_t4096")
+    # the oracle runs on the host: draw the inputs on the GPU when there is one (fast), then copy
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = inputs.make_experts(w, dev)
+    x = inputs.make_x(w, dev)
+    Wg, _ = inputs.make_router(w, dev)
+    per_step = []
+    res = None
+    for i in range(args.warmup + args.steps):
+        res = time_oracle(x, Wg, W, budget_s=args.ref_budget_s, min_tokens=1, seed=i)
+        if i >= args.warmup:
+            per_step.append(res)
+    tok_s = sum(r["tokens"] for r in per_step) / sum(r["seconds"] for r in per_step)
+    ms_per_step = w.T / tok_s * 1e3
+    cb = cpu_baseline_block(dict(res, tok_s=tok_s, tokens=sum(r["tokens"] for r in per_step),
+                                 seconds=sum(r["seconds"] for r in per_step)), w.T)
+    return {"impl": "reference", "metric": METRIC, "value": round(tok_s, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0, 1/sqrt(fan_in)) weights, unit-RMS x)",
+            "config": {"workload": "prefill_t4096", "T": w.T, "d": w.d, "d_ff": w.d_ff, "n_experts": w.n_experts,
+                       "k": w.k, "parallelism": "host cores (OpenMP over tokens)",
+                       "sample": "each step: a bounded seeded sample of the T=4096 tokens"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(tok_s, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=6.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
+    line, host = run_ours(args, rank, world, dist)
+    if rank == 0:
+        if host is not None:
+            res = time_oracle(host["x"], host["Wg"], host["W"], budget_s=args.cpu_budget_s, min_tokens=8)
+            line["cpu_baseline"] = cpu_baseline_block(res, 4096)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * moe.h -- C ABI of the Mixtral sparse mixture-of-experts feed-forward layer
+ *          on B300 (sm_103a).  Library: sparse_mixture_experts_54_b300/libmoe_b300.so
+ *
+ * The layer (Mixtral of Experts, section 2.1; restated in "从Mistral 7B到MoE模型
+ * Mixtral 8x7B的全面解析" (aiqianji) section 2.1.1 and in the xyznot summary,
+ * "Method"):
+ *
+ *     y = sum_{i=0}^{n-1} Softmax(TopK(x . W_g))_i * SwiGLU_i(x),
+ *     SwiGLU_i(x) = W2_i ( SiLU(W1_i x) * (W3_i x) ),   SiLU(z) = z / (1 + e^-z)
+ *
+ * with TopK keeping the K largest router logits and setting the rest to -inf,
+ * so only K experts per token are evaluated.  Mixtral: d = 4096, d_ff = 14336,
+ * n = 8, K = 2.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Layouts are row-major, nn.Linear style ([out][in]), as in the router
+ *    `nn.Linear(hidden_dim, num_experts, bias=False)` (aiqianji 2.1.4) and the
+ *    expert's w1/w3/w2 linears (aiqianji 3.2.4, code block D):
+ *        x   [T][d]            element type = context dtype
+ *        W_g [n][d]            fp32 always
+ *        W1  [n][d_ff][d]      element type = context dtype
+ *        W3  [n][d_ff][d]
+ *        W2  [n][d][d_ff]
+ *        y   [T][d]            element type = context dtype
+ *  - Pointers named "device" must point to device memory of the current CUDA
+ *    device and be 16-byte aligned.  The caller owns every pointer and the
+ *    stream; the library never frees caller memory.
+ *  - All compute entry points are asynchronous on `stream` and do not
+ *    synchronise the host.  Argument errors are returned synchronously
+ *    (moe_status_t).  Failures inside kernels (a bounded wait that ran out, a
+ *    failed debug bounds check) are recorded in a sticky status word that
+ *    moe_status() reads without synchronising.
+ *  - A context must not be used from two host threads at once; calls on
+ *    different streams with the same context share its workspace and must be
+ *    ordered by the caller.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx;
+/* Same object as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = -1,      /* bad argument (NULL pointer, T < 0, misaligned pointer, ...) */
+    MOE_ERR_CUDA = -2,         /* a CUDA runtime call or kernel launch failed */
+    MOE_ERR_OOM = -3,          /* workspace allocation failed */
+    MOE_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (sticky, via moe_status) */
+    MOE_ERR_UNSUPPORTED = -5,  /* shape/dtype the kernels cannot tile */
+    MOE_ERR_BOUNDS = -6        /* a kernel-side index check failed (sticky, via moe_status) */
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype_t;
+
+/* Options for moe_set_option. */
+typedef enum {
+    MOE_OPT_DECODE_MAX_T = 1,  /* forward uses the weight-streaming decode kernels when T <= value (default 64) */
+    MOE_OPT_WAIT_LIMIT_US = 2, /* wall-time limit of every bounded wait inside a kernel (default 2,000,000 us) */
+    MOE_OPT_FORCE_PATH = 3,    /* 0 = choose by T, 1 = always grouped GEMM, 2 = always decode kernels */
+    MOE_OPT_STAGE_TIMING = 4   /* 1 = record CUDA events around every kernel of moe_forward (see moe_stage_times) */
+} moe_option_t;
+
+/*
+ * Create a layer context for hidden size d, expert hidden size d_ff, n_experts
+ * experts and top-k routing (Mixtral: 4096, 14336, 8, 2; the K/n trade-off is
+ * aiqianji 2.1.1).  Requires 1 <= k <= n_experts <= 32, d % 8 == 0, d_ff >= 1.
+ * Context dtype defaults to MOE_BF16.  Allocates only the host-mapped status
+ * word; the workspace grows on first use (or moe_reserve).  Returns NULL on bad
+ * arguments or when no CUDA device is usable.
+ */
+moe_ctx* moe_create(int d, int d_ff, int n_experts, int k);
+
+/* Element type of x, W1, W3, W2 and y: MOE_BF16 (default) or MOE_F32.
+ * bf16 additionally requires d % 256 == 0 and d_ff % 128 == 0 (tensor-core tiling);
+ * MOE_F32 runs CUDA-core FMA kernels (no TF32) for any shape. */
+int moe_set_dtype(moe_ctx* ctx, int dtype);
+
+/* Optional router bias b_g [n] fp32, device pointer, added to the logits before
+ * top-k and softmax; NULL removes it.  Mixtral's router has no bias
+ * (aiqianji 2.1.4); this exists for skewed-load workloads.  The pointer is
+ * kept, not copied: it must stay valid while the context uses it. */
+int moe_set_router_bias(moe_ctx* ctx, const float* b_g);
+
+int moe_set_option(moe_ctx* ctx, int option, long long value);
+
+/* Grow the workspace now for up to T_max tokens (no allocation happens later
+ * for T <= T_max, e.g. while a stream is being captured into a CUDA graph). */
+int moe_reserve(moe_ctx* ctx, int T_max);
+
+/* Device workspace bytes a call with T tokens needs. */
+size_t moe_workspace_bytes(const moe_ctx* ctx, int T);
+
+/*
+ * Routing and dispatch only (router logits, top-k gate, expert-contiguous order).
+ *   x [T][d] (device, context dtype), W_g [n][d] (device, fp32).
+ * Outputs (device; each may be NULL):
+ *   topk_idx [T][k] int32   experts by descending logit, equal logits -> lower index first
+ *   topk_w   [T][k] fp32    Softmax over the kept logits (aiqianji 2.1.1; equal to the
+ *                           renormalised top-k of the full softmax, aiqianji 3.1.1 steps 4-6)
+ *   counts   [n]    int32   assignments per expert
+ *   offsets  [n+1]  int32   exclusive scan of counts, offsets[n] = k*T
+ *   perm     [k*T]  int32   flat assignment number t*k+slot at each expert-contiguous
+ *                           position; stable (ascending t*k+slot within an expert), which
+ *                           lists each expert's tokens as the one_hot/where walk of
+ *                           aiqianji 3.1.2 and code blocks B/C does.
+ * T == 0 is valid and writes nothing but counts/offsets (all zero).
+ */
+int moe_route(moe_ctx* ctx, const void* x, const float* W_g, int T,
+              int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+              int32_t* perm, moe_stream_t stream);
+
+/* Router logits only: logits [T][n] fp32 (device) = x . W_g^T (+ bias), with the
+ * same fp32 arithmetic moe_route and moe_forward use. */
+int moe_router_logits(moe_ctx* ctx, const void* x, const float* W_g, int T, float* logits,
+                      moe_stream_t stream);
+
+/*
+ * The whole layer: y [T][d] = MoE(x).  All pointers device.  Steps (all CUDA
+ * kernels): router + top-k gate; dispatch (histogram, scan, stable scatter,
+ * row gather); expert W1/W3 GEMM with the SiLU(a)*b product fused; expert W2
+ * GEMM with the gate weight applied to each row (the gate multiplies the W2
+ * output inside the expert, aiqianji 3.2.4 code block D); and a combine that
+ * adds each token's k expert rows in slot order (replacing index_add_,
+ * aiqianji 3.1.2) with no atomics, so results are bitwise reproducible.
+ * bf16: fp32 accumulation, the SwiGLU product rounded once to bf16, y rounded
+ * once.  Small T (<= MOE_OPT_DECODE_MAX_T) uses weight-streaming kernels.
+ * x and y must not overlap.  T == 0 is a no-op.
+ */
+int moe_forward(moe_ctx* ctx, const void* x, const float* W_g, const void* W1, const void* W3,
+                const void* W2, void* y, int T, moe_stream_t stream);
+
+/*
+ * moe_forward with x and y in host memory (pinned memory gives asynchronous
+ * copies; pageable memory works but the copies then synchronise).  Copies x
+ * to a context-owned device buffer, runs the layer and copies y back, all on
+ * `stream`.  Weights stay device pointers.  The host buffers must stay valid
+ * until the stream reaches this point.
+ */
+int moe_forward_host(moe_ctx* ctx, const void* x_host, const float* W_g, const void* W1,
+                     const void* W3, const void* W2, void* y_host, int T, moe_stream_t stream);
+
+/* Sticky kernel-side status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BOUNDS) of every
+ * call so far; reads host-mapped memory, synchronises nothing.  Results written
+ * by kernels still running are not yet visible. */
+int moe_status(moe_ctx* ctx);
+/* Reset the sticky status to MOE_OK. */
+int moe_clear_status(moe_ctx* ctx);
+
+/* Self-test of the bounded-wait machinery: launches one kernel whose wait can
+ * never complete (nothing arrives on its barrier); it gives up after
+ * wait_limit_us microseconds, records MOE_ERR_TIMEOUT and returns normally. */
+int moe_selftest_wait_timeout(moe_ctx* ctx, long long wait_limit_us, moe_stream_t stream);
+
+/*
+ * Per-kernel device time of the moe_forward calls made since the last read,
+ * while MOE_OPT_STAGE_TIMING is on.  Events are recorded on the call's stream
+ * around each kernel, so they measure exactly the launches of that stream.
+ * Synchronises on the last recorded event, writes the mean milliseconds per
+ * call of each stage into ms[0..max_stages) (stage names: moe_stage_name) and
+ * the number of calls into *calls, then forgets the recorded calls.  Returns
+ * the number of stages (>= 0) or a negative moe_status_t.
+ */
+int moe_stage_times(moe_ctx* ctx, float* ms, int max_stages, int* calls);
+/* Name of stage i of moe_stage_times, or NULL past the last stage. */
+const char* moe_stage_name(int i);
+
+/* Human-readable name of a moe_status_t value. */
+const char* moe_error_string(int code);
+
+/* Release the context and its workspace.  NULL-safe.  The caller must have
+ * synchronised every stream that used the context. */
+void moe_destroy(moe_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

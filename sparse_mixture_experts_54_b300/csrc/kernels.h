@@ -1,0 +1,51 @@
+// kernels.h -- host-side launchers of the MoE kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Schedule block written by the dispatch kernel (int32, device):
+//   [0, n)          counts[e]
+//   [n, 2n+1)       offsets[e] (exclusive scan), offsets[n] = R
+//   [2n+1, 3n+2)    tile_prefix[e] = sum_{e'<e} ceil(counts[e'] / kTileM), tile_prefix[n] = total
+constexpr int kTileM = 128;
+inline int sched_ints(int n) { return 3 * n + 2; }
+
+enum class ElemType { BF16 = 0, F32 = 1 };
+
+// routing ---------------------------------------------------------------------
+cudaError_t launch_router(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d,
+                          int n, int K, int32_t* topk_idx, float* topk_w, float* logits, int num_sms,
+                          cudaStream_t s);
+cudaError_t launch_dispatch(const int32_t* topk_idx, int R, int n, int* sched, int32_t* perm,
+                            int32_t* inv, KStatus st, cudaStream_t s);
+cudaError_t launch_gather(ElemType et, const void* x, const int32_t* perm, int R, int K, int d,
+                          void* Xp, cudaStream_t s);
+cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, void* y, cudaStream_t s);
+
+// CUDA-core grouped GEMMs (fp32 path) ------------------------------------------
+cudaError_t launch_simt_gemm13(ElemType et, const void* Xp, const void* W1, const void* W3, void* H,
+                               const int* sched, int n, int d, int F, int R, cudaStream_t s);
+cudaError_t launch_simt_gemm2(ElemType et, const void* H, const void* W2, float* Ys, const int* sched,
+                              const int32_t* perm, const float* topk_w, int n, int d, int F, int R,
+                              cudaStream_t s);
+
+// tcgen05 grouped GEMMs (bf16 path) --------------------------------------------
+bool encode_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows);
+cudaError_t launch_tc_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1,
+                             const CUtensorMap& mapW3, const int* sched, int n, int d, int F, int R,
+                             __nv_bfloat16* H, KStatus st, int num_sms, cudaStream_t s);
+cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, const int* sched, int n,
+                            int d, int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
+                            KStatus st, int num_sms, cudaStream_t s);
+
+// self-test of the bounded waits -------------------------------------------------
+cudaError_t launch_wait_selftest(KStatus st, cudaStream_t s);
+
+}  // namespace moe

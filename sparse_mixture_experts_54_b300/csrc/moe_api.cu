@@ -1,0 +1,469 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: context, workspace and
+// the launch sequence of the MoE layer.
+#include <stdlib.h>
+#include <string.h>
+
+#include <array>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+using namespace moe;
+
+struct moe_ctx {
+    int d = 0, F = 0, n = 0, k = 0;
+    int dtype = MOE_BF16;
+    const float* bias = nullptr;
+    int decode_max_t = 0;
+    long long wait_limit_us = 2000000;
+    int force_path = 0;
+    int device = 0;
+    int num_sms = 148;
+    int* status_host = nullptr;   // host-mapped
+    int* status_dev = nullptr;    // device alias
+    // workspace (one allocation)
+    int cap_T = -1;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t* topk_idx = nullptr;
+    float* topk_w = nullptr;
+    int32_t* perm = nullptr;
+    int32_t* inv = nullptr;
+    int* sched = nullptr;
+    void* Xp = nullptr;
+    void* H = nullptr;
+    float* Ys = nullptr;
+    void* xbuf = nullptr;
+    void* ybuf = nullptr;
+    CUtensorMap map_Xp, map_H;
+    bool maps_ok = false;
+    // per-stage CUDA-event timing (MOE_OPT_STAGE_TIMING)
+    bool stage_timing = false;
+    std::vector<cudaEvent_t> ev_free;
+    std::vector<std::array<cudaEvent_t, 8>> ev_calls;
+};
+
+namespace {
+
+size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+    size_t topk_idx, topk_w, perm, inv, sched, Xp, H, Ys, xbuf, ybuf, total;
+};
+
+Layout layout_for(const moe_ctx* c, int T) {
+    Layout L{};
+    const size_t R = static_cast<size_t>(c->k) * static_cast<size_t>(T > 0 ? T : 1);
+    const size_t Tn = static_cast<size_t>(T > 0 ? T : 1);
+    const size_t es = esize(c->dtype);
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += align256(bytes); return o; };
+    L.topk_idx = take(R * 4);
+    L.topk_w = take(R * 4);
+    L.perm = take(R * 4);
+    L.inv = take(R * 4);
+    L.sched = take(static_cast<size_t>(sched_ints(c->n)) * 4);
+    L.Xp = take(R * c->d * es);
+    L.H = take(R * c->F * es);
+    L.Ys = take(R * c->d * 4);
+    L.xbuf = take(Tn * c->d * es);
+    L.ybuf = take(Tn * c->d * es);
+    L.total = off;
+    return L;
+}
+
+KStatus kstatus(const moe_ctx* c) {
+    KStatus st;
+    st.word = c->status_dev;
+    st.wait_ns = static_cast<uint64_t>(c->wait_limit_us) * 1000ull;
+    return st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA; }
+
+bool env_flag(const char* name) {
+    const char* v = getenv(name);
+    return v && *v && strcmp(v, "0") != 0;
+}
+
+// Make sure the workspace holds T tokens.  Growth frees the old buffer after
+// synchronising the stream; it is refused while the stream is being captured.
+int ensure_workspace(moe_ctx* c, int T, cudaStream_t s) {
+    if (T <= c->cap_T && c->ws) return MOE_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) return MOE_ERR_INVALID;
+    if (env_flag("MOE_FAIL_WORKSPACE_ALLOC")) return MOE_ERR_OOM;   // host-side fault injection for tests
+    Layout L = layout_for(c, T);
+    if (c->ws) {
+        cudaStreamSynchronize(s);
+        cudaDeviceSynchronize();
+        cudaFree(c->ws);
+        c->ws = nullptr;
+        c->cap_T = -1;
+        c->maps_ok = false;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, L.total);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_OOM;
+    }
+    char* b = static_cast<char*>(p);
+    c->ws = p;
+    c->ws_bytes = L.total;
+    c->topk_idx = reinterpret_cast<int32_t*>(b + L.topk_idx);
+    c->topk_w = reinterpret_cast<float*>(b + L.topk_w);
+    c->perm = reinterpret_cast<int32_t*>(b + L.perm);
+    c->inv = reinterpret_cast<int32_t*>(b + L.inv);
+    c->sched = reinterpret_cast<int*>(b + L.sched);
+    c->Xp = b + L.Xp;
+    c->H = b + L.H;
+    c->Ys = reinterpret_cast<float*>(b + L.Ys);
+    c->xbuf = b + L.xbuf;
+    c->ybuf = b + L.ybuf;
+    c->cap_T = T;
+    // Tensor maps of the workspace activations cover the full capacity; rows
+    // beyond the live K*T are never valid rows of any tile.
+    if (c->dtype == MOE_BF16) {
+        const uint64_t R = static_cast<uint64_t>(c->k) * static_cast<uint64_t>(T > 0 ? T : 1);
+        c->maps_ok = encode_map_bf16_2d(&c->map_Xp, c->Xp, R, c->d, 128) &&
+                     encode_map_bf16_2d(&c->map_H, c->H, R, c->F, 128);
+        if (!c->maps_ok) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+bool tc_shape_ok(const moe_ctx* c) { return c->d % 256 == 0 && c->F % 128 == 0; }
+
+// Stages of one forward call, in launch order.
+constexpr int kStages = 6;
+const char* const kStageNames[kStages] = {"router", "dispatch", "gather", "expert_w1w3_swiglu",
+                                          "expert_w2_gate", "combine"};
+
+// Events of the current call when stage timing is on (null otherwise).
+struct StageMarks {
+    moe_ctx* c = nullptr;
+    cudaStream_t s = nullptr;
+    std::array<cudaEvent_t, 8> ev{};
+    bool on = false;
+    StageMarks(moe_ctx* ctx, cudaStream_t st) : c(ctx), s(st) {
+        if (!c->stage_timing) return;
+        for (int i = 0; i <= kStages; ++i) {
+            if (!c->ev_free.empty()) {
+                ev[i] = c->ev_free.back();
+                c->ev_free.pop_back();
+            } else if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+                for (int j = 0; j < i; ++j) c->ev_free.push_back(ev[j]);
+                return;
+            }
+        }
+        on = true;
+        cudaEventRecord(ev[0], s);
+    }
+    void mark(int stage) {
+        if (on) cudaEventRecord(ev[stage + 1], s);
+    }
+    void finish() {
+        if (on) {
+            c->ev_calls.push_back(ev);
+            on = false;
+        }
+    }
+    ~StageMarks() {
+        if (on)
+            for (int i = 0; i <= kStages; ++i) c->ev_free.push_back(ev[i]);
+    }
+};
+
+// router + top-k + dispatch into the workspace
+int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s, float* logits) {
+    const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
+    const int R = c->k * T;
+    cudaError_t e = launch_router(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, logits,
+                                  c->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_dispatch(c->topk_idx, R, c->n, c->sched, c->perm, c->inv, kstatus(c), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MOE_OK;
+}
+
+int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
+                int T, cudaStream_t s) {
+    const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
+    const int R = c->k * T;
+    StageMarks marks(c, s);
+    cudaError_t e = launch_router(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, nullptr,
+                                  c->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(0);
+    e = launch_dispatch(c->topk_idx, R, c->n, c->sched, c->perm, c->inv, kstatus(c), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(1);
+    e = launch_gather(et, x, c->perm, R, c->k, c->d, c->Xp, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(2);
+    if (et == ElemType::F32) {
+        e = launch_simt_gemm13(et, c->Xp, W1, W3, c->H, c->sched, c->n, c->d, c->F, R, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(3);
+        e = launch_simt_gemm2(et, c->H, W2, c->Ys, c->sched, c->perm, c->topk_w, c->n, c->d, c->F, R, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(4);
+    } else {
+        CUtensorMap mW1, mW3, mW2;
+        const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
+        if (!encode_map_bf16_2d(&mW1, W1, nF, c->d, 128) || !encode_map_bf16_2d(&mW3, W3, nF, c->d, 128) ||
+            !encode_map_bf16_2d(&mW2, W2, nd, c->F, 256))
+            return MOE_ERR_CUDA;
+        const KStatus st = kstatus(c);
+        e = launch_tc_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
+                             static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(3);
+        e = launch_tc_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, st,
+                            c->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(4);
+    }
+    e = launch_combine(et, c->Ys, T, c->k, c->d, y, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(5);
+    marks.finish();
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_ctx* moe_create(int d, int d_ff, int n_experts, int k) {
+    if (d <= 0 || d % 8 != 0 || d_ff <= 0 || n_experts < 1 || n_experts > 32 || k < 1 || k > n_experts) return nullptr;
+    // the router stages W_g [n][d] fp32 in shared memory
+    if (static_cast<size_t>(n_experts) * d * 4 > 200 * 1024) return nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    moe_ctx* c = new moe_ctx();
+    c->d = d;
+    c->F = d_ff;
+    c->n = n_experts;
+    c->k = k;
+    c->device = dev;
+    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (c->num_sms <= 0) c->num_sms = 148;
+    if (const char* v = getenv("MOE_WAIT_LIMIT_US")) c->wait_limit_us = atoll(v) > 0 ? atoll(v) : c->wait_limit_us;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&c->status_host), sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->status_dev), c->status_host, 0) != cudaSuccess) {
+        cudaGetLastError();
+        if (c->status_host) cudaFreeHost(c->status_host);
+        delete c;
+        return nullptr;
+    }
+    *c->status_host = 0;
+    return c;
+}
+
+int moe_set_dtype(moe_ctx* c, int dtype) {
+    if (!c || (dtype != MOE_BF16 && dtype != MOE_F32)) return MOE_ERR_INVALID;
+    if (dtype != c->dtype) {
+        if (c->ws) {
+            cudaDeviceSynchronize();
+            cudaFree(c->ws);
+            c->ws = nullptr;
+            c->cap_T = -1;
+            c->maps_ok = false;
+        }
+        c->dtype = dtype;
+    }
+    return MOE_OK;
+}
+
+int moe_set_router_bias(moe_ctx* c, const float* b) {
+    if (!c) return MOE_ERR_INVALID;
+    if (b && !aligned16(b)) return MOE_ERR_INVALID;
+    c->bias = b;
+    return MOE_OK;
+}
+
+int moe_set_option(moe_ctx* c, int option, long long value) {
+    if (!c) return MOE_ERR_INVALID;
+    switch (option) {
+        case MOE_OPT_DECODE_MAX_T:
+            if (value < 0) return MOE_ERR_INVALID;
+            c->decode_max_t = static_cast<int>(value);
+            return MOE_OK;
+        case MOE_OPT_WAIT_LIMIT_US:
+            if (value <= 0) return MOE_ERR_INVALID;
+            c->wait_limit_us = value;
+            return MOE_OK;
+        case MOE_OPT_FORCE_PATH:
+            if (value < 0 || value > 2) return MOE_ERR_INVALID;
+            c->force_path = static_cast<int>(value);
+            return MOE_OK;
+        case MOE_OPT_STAGE_TIMING:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID;
+            c->stage_timing = value != 0;
+            return MOE_OK;
+        default:
+            return MOE_ERR_INVALID;
+    }
+}
+
+size_t moe_workspace_bytes(const moe_ctx* c, int T) {
+    if (!c || T < 0) return 0;
+    return layout_for(c, T).total;
+}
+
+int moe_reserve(moe_ctx* c, int T_max) {
+    if (!c || T_max < 0) return MOE_ERR_INVALID;
+    return ensure_workspace(c, T_max, nullptr);
+}
+
+int moe_route(moe_ctx* c, const void* x, const float* Wg, int T, int32_t* topk_idx, float* topk_w, int32_t* counts,
+              int32_t* offsets, int32_t* perm, moe_stream_t stream) {
+    if (!c || T < 0) return MOE_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T > 0 && (!x || !Wg || !aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID;
+    int rc = ensure_workspace(c, T, s);
+    if (rc != MOE_OK) return rc;
+    if (T > 0) {
+        rc = run_route(c, x, Wg, T, s, nullptr);
+        if (rc != MOE_OK) return rc;
+    } else {
+        if (cudaMemsetAsync(c->sched, 0, sched_ints(c->n) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    const size_t R = static_cast<size_t>(c->k) * T;
+    cudaError_t e = cudaSuccess;
+    if (topk_idx && R) e = cudaMemcpyAsync(topk_idx, c->topk_idx, R * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && topk_w && R) e = cudaMemcpyAsync(topk_w, c->topk_w, R * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && counts) e = cudaMemcpyAsync(counts, c->sched, c->n * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && offsets)
+        e = cudaMemcpyAsync(offsets, c->sched + c->n, (c->n + 1) * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && perm && R) e = cudaMemcpyAsync(perm, c->perm, R * 4, cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_router_logits(moe_ctx* c, const void* x, const float* Wg, int T, float* logits, moe_stream_t stream) {
+    if (!c || T < 0) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    if (!x || !Wg || !logits || !aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = ensure_workspace(c, T, s);
+    if (rc != MOE_OK) return rc;
+    const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
+    cudaError_t e = launch_router(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, logits,
+                                  c->num_sms, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int moe_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
+                int T, moe_stream_t stream) {
+    if (!c || T < 0) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    if (!x || !Wg || !W1 || !W3 || !W2 || !y) return MOE_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(y))
+        return MOE_ERR_INVALID;
+    if (c->dtype == MOE_BF16 && !tc_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = ensure_workspace(c, T, s);
+    if (rc != MOE_OK) return rc;
+    return run_forward(c, x, Wg, W1, W3, W2, y, T, s);
+}
+
+int moe_forward_host(moe_ctx* c, const void* x_host, const float* Wg, const void* W1, const void* W3, const void* W2,
+                     void* y_host, int T, moe_stream_t stream) {
+    if (!c || T < 0) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    if (!x_host || !y_host) return MOE_ERR_INVALID;
+    if (!Wg || !W1 || !W3 || !W2) return MOE_ERR_INVALID;
+    if (c->dtype == MOE_BF16 && !tc_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = ensure_workspace(c, T, s);
+    if (rc != MOE_OK) return rc;
+    const size_t bytes = static_cast<size_t>(T) * c->d * esize(c->dtype);
+    if (cudaMemcpyAsync(c->xbuf, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+    rc = run_forward(c, c->xbuf, Wg, W1, W3, W2, c->ybuf, T, s);
+    if (rc != MOE_OK) return rc;
+    if (cudaMemcpyAsync(y_host, c->ybuf, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_status(moe_ctx* c) {
+    if (!c) return MOE_ERR_INVALID;
+    const int w = *reinterpret_cast<volatile int*>(c->status_host);
+    if (w & kStatusTimeout) return MOE_ERR_TIMEOUT;
+    if (w & kStatusBounds) return MOE_ERR_BOUNDS;
+    return MOE_OK;
+}
+
+int moe_clear_status(moe_ctx* c) {
+    if (!c) return MOE_ERR_INVALID;
+    *reinterpret_cast<volatile int*>(c->status_host) = 0;
+    return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(moe_ctx* c, long long wait_limit_us, moe_stream_t stream) {
+    if (!c || wait_limit_us <= 0 || wait_limit_us > 10000000) return MOE_ERR_INVALID;
+    KStatus st = kstatus(c);
+    st.wait_ns = static_cast<uint64_t>(wait_limit_us) * 1000ull;
+    cudaError_t e = launch_wait_selftest(st, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_stage_times(moe_ctx* c, float* ms, int max_stages, int* calls) {
+    if (!c || (max_stages > 0 && !ms)) return MOE_ERR_INVALID;
+    const int ncalls = static_cast<int>(c->ev_calls.size());
+    if (calls) *calls = ncalls;
+    double sum[kStages] = {0};
+    int rc = kStages;
+    if (ncalls > 0) {
+        if (cudaEventSynchronize(c->ev_calls.back()[kStages]) != cudaSuccess) rc = MOE_ERR_CUDA;
+        for (auto& ev : c->ev_calls) {
+            for (int i = 0; i < kStages && rc >= 0; ++i) {
+                float t = 0.0f;
+                if (cudaEventElapsedTime(&t, ev[i], ev[i + 1]) != cudaSuccess) rc = MOE_ERR_CUDA;
+                sum[i] += t;
+            }
+            for (int i = 0; i <= kStages; ++i) c->ev_free.push_back(ev[i]);
+        }
+        c->ev_calls.clear();
+    }
+    if (rc < 0) {
+        cudaGetLastError();
+        return rc;
+    }
+    for (int i = 0; i < kStages && i < max_stages; ++i) ms[i] = ncalls ? static_cast<float>(sum[i] / ncalls) : 0.0f;
+    return kStages;
+}
+
+const char* moe_stage_name(int i) { return (i >= 0 && i < kStages) ? kStageNames[i] : nullptr; }
+
+const char* moe_error_string(int code) {
+    switch (code) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID: return "MOE_ERR_INVALID";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_OOM: return "MOE_ERR_OOM";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+void moe_destroy(moe_ctx* c) {
+    if (!c) return;
+    for (auto& ev : c->ev_calls) c->ev_free.insert(c->ev_free.end(), ev.begin(), ev.begin() + kStages + 1);
+    for (cudaEvent_t e : c->ev_free) cudaEventDestroy(e);
+    if (c->ws) cudaFree(c->ws);
+    if (c->status_host) cudaFreeHost(c->status_host);
+    delete c;
+}
+
+}  // extern "C"

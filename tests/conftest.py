@@ -29,3 +29,17 @@ def read_golden(name):
             except ValueError:
                 keyed[parts[0]] = [float(p) for p in parts[1:]]
     return keyed, rows
+
+
+def pytest_collection_modifyitems(config, items):
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:
+        has_gpu = False
+    if has_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)

@@ -1,0 +1,151 @@
+"""The whole MoE layer on the GPU (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import assert_close, check_route, near_tie_mask, reference_selection, y_to_numpy
+from sparse_mixture_experts_54_b300 import _lib, inputs
+from sparse_mixture_experts_54_b300.layer import MoELayer
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_y(layer, w, toks, gpu_idx):
+    x, Wg, W1, W3, W2, b = (inputs.to_oracle(layer[k]) for k in ("x", "Wg", "W1", "W3", "W2", "bias"))
+    logits = oracle.router_logits(x, Wg, b)
+    idx, gate = oracle.select_topk(logits, w.k)
+    ref = dict(logits=logits, idx=idx, gate=gate)
+    idx_u, gate_u, near = reference_selection(ref, gpu_idx, w.k)
+    y = oracle.moe_tokens(x, W1, W3, W2, idx_u, gate_u, toks)
+    return y, ref, near
+
+
+def run_layer(w, layer, path=0):
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, dtype=w.torch_dtype, bias=layer["bias"])
+    if path:
+        m.set_option(_lib.MOE_OPT_FORCE_PATH, path)
+    r = m.route(layer["x"], layer["Wg"])
+    y = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
+    torch.cuda.synchronize()
+    assert m.status() == 0, _lib.moe_error_string(m.status())
+    return m, y, r["topk_idx"].cpu().numpy(), r["topk_w"].cpu().numpy()
+
+
+def test_tiny_fp32_full_parity():
+    w = inputs.workload("tiny_fp32")
+    layer = inputs.make_layer(w, "cuda")
+    m, y, gidx, gw = run_layer(w, layer)
+    y_ref, ref, near = oracle_y(layer, w, np.arange(w.T), gidx)
+    check_route(gidx, gw, ref["logits"], ref["idx"], ref["gate"], w.k)
+    err, bound = assert_close(y_to_numpy(y), y_ref, "f32")
+    print(f"tiny fp32: max err {err:.3e} (bound {bound:.3e}), near ties {near}")
+
+
+SMALL_BF16 = [
+    # T, d, F, n, K
+    (1, 256, 128, 8, 2),
+    (5, 256, 256, 8, 2),
+    (64, 256, 384, 8, 2),
+    (129, 512, 256, 8, 2),
+    (1000, 512, 384, 8, 2),
+    (300, 256, 256, 4, 1),
+    (257, 256, 256, 8, 3),
+    (200, 768, 640, 16, 2),
+]
+
+
+@pytest.mark.parametrize("T,d,F,n,K", SMALL_BF16)
+def test_bf16_small_shapes(T, d, F, n, K):
+    w = inputs.Workload("small", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=T + d)
+    layer = inputs.make_layer(w, "cuda")
+    m, y, gidx, gw = run_layer(w, layer)
+    y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
+    check_route(gidx, gw, ref["logits"], ref["idx"], ref["gate"], K)
+    assert_close(y_to_numpy(y), y_ref, "bf16")
+
+
+def test_bf16_all_tokens_one_expert_pair():
+    # every token to experts (5, 2): one group of 700 rows (6 tiles, ragged), all other experts empty
+    w = inputs.Workload("skew", T=700, d=256, d_ff=256, bias=(0, 0, 50, 0, 0, 100, 0, 0), seed=3)
+    layer = inputs.make_layer(w, "cuda")
+    m, y, gidx, gw = run_layer(w, layer)
+    assert np.all(gidx == [5, 2])
+    y_ref, ref, near = oracle_y(layer, w, np.arange(w.T), gidx)
+    assert_close(y_to_numpy(y), y_ref, "bf16")
+
+
+def test_bf16_fp32_fallback_shape_rejected():
+    m = MoELayer(200, 256, 8, 2)   # d not a multiple of 256: no tensor-core tiling
+    x = torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda")
+    Wg = torch.zeros((8, 200), dtype=torch.float32, device="cuda")
+    W = torch.zeros((8, 256, 200), dtype=torch.bfloat16, device="cuda")
+    W2 = torch.zeros((8, 200, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(_lib.MoEError) as ei:
+        m.forward(x, Wg, W, W, W2)
+    assert ei.value.code == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_empty_batch_is_noop():
+    w = inputs.workload("tiny_fp32")
+    layer = inputs.make_layer(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, dtype=torch.float32)
+    x = torch.empty((0, w.d), dtype=torch.float32, device="cuda")
+    y = m.forward(x, layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
+    torch.cuda.synchronize()
+    assert y.shape == (0, w.d) and m.status() == 0
+
+
+def test_forward_is_bitwise_deterministic_and_host_entry_matches():
+    w = inputs.Workload("det", T=1000, d=512, d_ff=384, seed=11)
+    layer = inputs.make_layer(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    y1 = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"]).clone()
+    y2 = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"]).clone()
+    xh = layer["x"].cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    m.forward_host(xh, layer["Wg"], layer["W1"], layer["W3"], layer["W2"], yh)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert torch.equal(y1.cpu(), yh)
+    assert m.status() == 0
+
+
+# ----------------------------------------------------------------------------- Mixtral shape
+@pytest.fixture(scope="module")
+def mixtral_experts():
+    w = inputs.workload("decode_t32")
+    W1, W3, W2 = inputs.make_experts(w, "cuda")
+    host = tuple(inputs.to_oracle(t) for t in (W1, W3, W2))
+    return (W1, W3, W2), host
+
+
+def _mixtral_case(name, mixtral_experts, sample, path=0):
+    w = inputs.workload(name)
+    (W1, W3, W2), (h1, h3, h2) = mixtral_experts
+    x = inputs.make_x(w, "cuda")
+    Wg, b = inputs.make_router(w, "cuda")
+    layer = dict(x=x, Wg=Wg, bias=b, W1=W1, W3=W3, W2=W2)
+    m, y, gidx, gw = run_layer(w, layer, path)
+    toks = inputs.sample_tokens(w.T, sample).numpy()
+    xo, Wgo, bo = inputs.to_oracle(x), inputs.to_oracle(Wg), inputs.to_oracle(b)
+    logits = oracle.router_logits(xo, Wgo, bo)
+    idx, gate = oracle.select_topk(logits, w.k)
+    near = check_route(gidx, gw, logits, idx, gate, w.k)
+    idx_u, gate_u, _ = reference_selection(dict(logits=logits, idx=idx, gate=gate), gidx, w.k)
+    y_ref = oracle.moe_tokens(xo, h1, h3, h2, idx_u, gate_u, toks)
+    err, bound = assert_close(y_to_numpy(y)[toks], y_ref, "bf16")
+    print(f"{name}: {len(toks)} tokens checked, max err {err:.3e} (bound {bound:.3e}), near ties {near}")
+    m.close()
+
+
+def test_mixtral_decode_t32_full(mixtral_experts):
+    _mixtral_case("decode_t32", mixtral_experts, 32)
+
+
+def test_mixtral_prefill_t4096_sampled(mixtral_experts):
+    _mixtral_case("prefill_t4096", mixtral_experts, 48)
+
+
+def test_mixtral_skewed_t32768_sampled(mixtral_experts):
+    _mixtral_case("skewed_t32768", mixtral_experts, 48)
