@@ -4,7 +4,8 @@ Tolerances (from the layer's arithmetic):
   * routing indices and dispatch order: bit-exact, except near-tie tokens whose
     fp64 oracle logits have two neighbours among the top K+1 closer than 1e-6
     (fp32 on the GPU may order them either way); those are counted;
-  * bf16: max|y - y_ref| <= 1e-2 * rms(y_ref);
+  * bf16: max|y - y_ref| <= 1e-2 * rms(y_ref), on top of the rounding of the
+    stored bf16 result itself (at most half an ulp, <= 2^-8 |y_ref|, elementwise);
   * fp32: max|y - y_ref| <= 1e-5 * max|y_ref|.
 """
 from __future__ import annotations
@@ -67,15 +68,21 @@ def reference_selection(ref: dict, gpu_idx: np.ndarray, K: int):
     return idx, gate, int(near.sum())
 
 
+BF16_STORE = 2.0 ** -8   # half an ulp of bf16, relative
+
+
 def assert_close(y_gpu: np.ndarray, y_ref: np.ndarray, dtype: str):
+    """Returns (max error beyond the output's own storage rounding, bound)."""
     y_gpu = y_gpu.astype(np.float64)
-    err = np.max(np.abs(y_gpu - y_ref))
+    assert np.all(np.isfinite(y_gpu)), "non-finite output"
+    diff = np.abs(y_gpu - y_ref)
     if dtype == "f32":
         bound = F32_TOL * np.max(np.abs(y_ref))
+        err = np.max(diff)
     else:
         bound = BF16_TOL * np.sqrt(np.mean(y_ref ** 2))
-    assert np.all(np.isfinite(y_gpu)), "non-finite output"
-    assert err <= bound, f"max abs err {err:.3e} > bound {bound:.3e}"
+        err = np.max(diff - BF16_STORE * np.abs(y_ref))
+    assert err <= bound, f"max abs err {err:.3e} > bound {bound:.3e} (raw max {np.max(diff):.3e})"
     return err, bound
 
 
