@@ -57,7 +57,8 @@ typedef enum {
     MOE_ERR_OOM = -3,          /* workspace allocation failed */
     MOE_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (sticky, via moe_status) */
     MOE_ERR_UNSUPPORTED = -5,  /* shape/dtype the kernels cannot tile */
-    MOE_ERR_BOUNDS = -6        /* a kernel-side index check failed (sticky, via moe_status) */
+    MOE_ERR_BOUNDS = -6,       /* a kernel-side index check failed (sticky, via moe_status) */
+    MOE_ERR_SCRATCH_LIMIT = -7 /* moe_forward_noalloc: the call needs more than its fixed scratch */
 } moe_status_t;
 
 typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype_t;
@@ -173,6 +174,40 @@ int moe_selftest_wait_timeout(moe_ctx* ctx, long long wait_limit_us, moe_stream_
 int moe_stage_times(moe_ctx* ctx, float* ms, int max_stages, int* calls);
 /* Name of stage i of moe_stage_times, or NULL past the last stage. */
 const char* moe_stage_name(int i);
+
+/*
+ * moe_forward_noalloc -- the same layer as moe_forward, for callers that
+ * cannot call cudaMalloc: it allocates nothing, on the device or the host, and
+ * needs no context (creating one allocates).  The pages have no counterpart to
+ * this entry point; it exists for processes whose device memory is owned and
+ * budgeted by another allocator, or that must not allocate once they are
+ * serving.
+ *
+ *  - Scratch: one fixed 32 MiB __device__ array inside this library.  Every GPU
+ *    that loads the library holds it until the process exits.  A call needs
+ *    256-byte-rounded regions of 4*k*T bytes (four of them), (3n+2)*4 bytes,
+ *    k*T*d*es, k*T*d_ff*es and k*T*d*4 bytes (es = 2 for bf16, 4 for fp32);
+ *    if their sum exceeds 32 MiB it returns MOE_ERR_SCRATCH_LIMIT and launches
+ *    nothing.  At the Mixtral shape (bf16, d=4096, d_ff=14336, k=2) that allows
+ *    T <= 314.
+ *  - Every call uses the same array, and each call overwrites the parts it
+ *    uses before reading them (nothing has to start at zero).  Calls that can
+ *    overlap on the GPU (different streams, different host threads, several
+ *    layers in flight) race on it: order them on one stream.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture.
+ *  - Arguments: as moe_forward, plus the shape (d, d_ff, n_experts, k), the
+ *    element type (moe_dtype_t) and an optional router bias b_g [n] (device,
+ *    fp32, NULL for none).  status, if not NULL, is a caller-owned device int
+ *    into which kernels OR their failure bits (1 = a bounded wait ran out,
+ *    2 = an index check failed); bounded waits give up after 2 s.  Returns
+ *    MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_SCRATCH_LIMIT or
+ *    MOE_ERR_CUDA; asynchronous like moe_forward.
+ */
+int moe_forward_noalloc(const void* x, const float* W_g, const float* b_g, const void* W1,
+                        const void* W3, const void* W2, void* y, int T, int d, int d_ff,
+                        int n_experts, int k, int dtype, int* status, moe_stream_t stream);
 
 /* Human-readable name of a moe_status_t value. */
 const char* moe_error_string(int code);

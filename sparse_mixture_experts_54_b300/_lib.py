@@ -21,6 +21,7 @@ MOE_ERR_OOM = -3
 MOE_ERR_TIMEOUT = -4
 MOE_ERR_UNSUPPORTED = -5
 MOE_ERR_BOUNDS = -6
+MOE_ERR_SCRATCH_LIMIT = -7
 
 MOE_BF16 = 0
 MOE_F32 = 1
@@ -48,6 +49,7 @@ SIGNATURES = {
     "moe_status": (_I, [_P]),
     "moe_clear_status": (_I, [_P]),
     "moe_selftest_wait_timeout": (_I, [_P, _LL, _P]),
+    "moe_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_stage_times": (_I, [_P, _P, _I, _P]),
     "moe_stage_name": (ctypes.c_char_p, [_I]),
     "moe_error_string": (ctypes.c_char_p, [_I]),
@@ -147,6 +149,11 @@ def moe_clear_status(ctx) -> int:
 
 def moe_selftest_wait_timeout(ctx, wait_limit_us: int, stream) -> int:
     return load().moe_selftest_wait_timeout(ctx, wait_limit_us, _p(stream))
+
+
+def moe_forward_noalloc(x, W_g, b_g, W1, W3, W2, y, T, d, d_ff, n_experts, k, dtype, status, stream) -> int:
+    return load().moe_forward_noalloc(_p(x), _p(W_g), _p(b_g), _p(W1), _p(W3), _p(W2), _p(y), T, d, d_ff,
+                                      n_experts, k, dtype, _p(status), _p(stream))
 
 
 def moe_stage_times(ctx, ms, max_stages: int, calls) -> int:

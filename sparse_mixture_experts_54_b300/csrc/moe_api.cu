@@ -453,6 +453,7 @@ const char* moe_error_string(int code) {
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
         case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
         case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS";
+        case MOE_ERR_SCRATCH_LIMIT: return "MOE_ERR_SCRATCH_LIMIT";
         default: return "MOE_ERR_UNKNOWN";
     }
 }
