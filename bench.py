@@ -78,7 +78,10 @@ def max_over_ranks(v: float, dist) -> float:
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every 200 ms) of SM clock, power and throttle reasons.
+
+    Samples are timestamped on arrival; summary() keeps those that arrived inside
+    the timed windows marked with window()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -88,6 +91,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.windows = []
 
     def __enter__(self):
         try:
@@ -102,7 +106,15 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def wait_first(self, timeout_s: float = 5.0):
+        t0 = time.monotonic()
+        while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout_s:
+            time.sleep(0.05)
+
+    def window(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -113,23 +125,28 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
+        sm, smax, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        inside = [l for (t, l) in self.lines if any(a <= t <= b + 0.25 for a, b in self.windows)]
+        for line in inside:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
                 sm.append(float(parts[0]))
                 smax = float(parts[1])
+                power.append(float(parts[2]))
             except ValueError:
                 continue
             for name, flag in zip(names, parts[4:8]):
                 if flag.lower() == "active":
                     reasons.add(name)
+        timed_s = sum(b - a for a, b in self.windows)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "timed_seconds": round(timed_s, 3), "note": "no nvidia-smi sample inside the timed region"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(power) if power else None, "timed_seconds": round(timed_s, 3)}
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -161,7 +178,7 @@ def run_ours(args, rank, world, dist):
     m.reserve(wp.T)
     stream = torch.cuda.current_stream()
 
-    def timed(x, steps, warmup, stage_timing):
+    def timed(x, steps, warmup, stage_timing, clk=None):
         for _ in range(warmup):
             m.forward(x, Wg, W1, W3, W2)
         torch.cuda.synchronize()
@@ -171,11 +188,14 @@ def run_ours(args, rank, world, dist):
         barrier(dist)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.monotonic()
         e0.record(stream)
         for _ in range(steps):
             m.forward(x, Wg, W1, W3, W2, y=y)
         e1.record(stream)
         torch.cuda.synchronize()
+        if clk is not None:
+            clk.window(t0, time.monotonic())
         barrier(dist)
         ms = e0.elapsed_time(e1) / steps
         stages, calls = m.stage_times()
@@ -190,8 +210,9 @@ def run_ours(args, rank, world, dist):
     counts_d = r["counts"].cpu().tolist()
 
     with ClockSampler(torch.cuda.current_device()) as clk:
-        ms_p, stages_p = timed(xp, args.steps, args.warmup, True)
-        ms_d, stages_d = timed(xd, max(args.steps, 10), args.warmup, True)
+        clk.wait_first()
+        ms_p, stages_p = timed(xp, args.steps, args.warmup, True, clk)
+        ms_d, stages_d = timed(xd, args.decode_steps, args.warmup, True, clk)
     clocks = clk.summary()
 
     # end to end: pinned host x in, host y out, through the host-buffer entry point
@@ -246,6 +267,8 @@ def run_ours(args, rank, world, dist):
                 "d2h_bytes_per_step": int(yh.numel() * yh.element_size()),
                 "ms_per_step": round(ms_e2e, 4), "entry_point": "moe_forward_host"},
         "gpu_launches": 6 * args.steps,
+        "timing": {"prefill_steps": args.steps, "decode_steps": args.decode_steps,
+                   "per_kernel": "CUDA events recorded by the library around each kernel on the call's stream"},
         "clocks": clocks,
     }
     m.close()
@@ -322,16 +345,42 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(tok_s, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_step(args):
+    """A few untimed forward calls of one workload, for ncu captures (no timing, no oracle)."""
+    from sparse_mixture_experts_54_b300 import _lib, inputs
+    from sparse_mixture_experts_54_b300.layer import MoELayer
+
+    torch.cuda.set_device(0)
+    w = inputs.workload(args.profile_step)
+    W1, W3, W2 = inputs.make_experts(w, "cuda")
+    x = inputs.make_x(w, "cuda")
+    Wg, b = inputs.make_router(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=b)
+    if args.force_path:
+        m.set_option(_lib.MOE_OPT_FORCE_PATH, args.force_path)
+    for _ in range(args.warmup + 1):
+        m.forward(x, Wg, W1, W3, W2)
+    torch.cuda.synchronize()
+    assert m.status() == 0
+    print(f"profile_step {w.name}: {args.warmup + 1} forward calls done", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--decode-steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=6.0)
+    ap.add_argument("--profile-step", default=None, help="workload name: run warmup+1 untimed calls (for ncu)")
+    ap.add_argument("--force-path", type=int, default=0)
     args = ap.parse_args()
+    if args.profile_step:
+        profile_step(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
 

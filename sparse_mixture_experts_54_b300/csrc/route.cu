@@ -11,13 +11,149 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Router: one warp per token.  W_g [n][d] fp32 is staged once per block in
-// shared memory; each lane owns 8 consecutive elements of every 256-element
-// slice of the row, sums its partial dot products in a fixed order and the
-// warp adds the lanes with a butterfly, so every lane holds all n logits and
-// the result does not depend on timing.
+// 8 consecutive elements of a row as fp32 (zeros past the end of the row).
+template <typename TX>
+__device__ __forceinline__ void load8(const TX* row, int j0, int d, float (&v)[8]) {
+    if (j0 >= d) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = 0.0f;
+        return;
+    }
+    if constexpr (sizeof(TX) == 2) {
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + j0));
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __bfloat162float(h[u]);
+    } else {
+        float4 a = __ldg(reinterpret_cast<const float4*>(row + j0));
+        float4 b = __ldg(reinterpret_cast<const float4*>(row + j0 + 4));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// acc + sum_u x[u] * w[u] over 8 elements, fused multiply-adds in index order.
+__device__ __forceinline__ float dot8(const float (&xv)[8], const float* w, float acc) {
+    float4 w0 = *reinterpret_cast<const float4*>(w);
+    float4 w1 = *reinterpret_cast<const float4*>(w + 4);
+    acc = fmaf(xv[0], w0.x, acc); acc = fmaf(xv[1], w0.y, acc);
+    acc = fmaf(xv[2], w0.z, acc); acc = fmaf(xv[3], w0.w, acc);
+    acc = fmaf(xv[4], w1.x, acc); acc = fmaf(xv[5], w1.y, acc);
+    acc = fmaf(xv[6], w1.z, acc); acc = fmaf(xv[7], w1.w, acc);
+    return acc;
+}
+
+// Top-k and gate from the n logits held (identically) by every lane of a warp:
+// lane e ranks its own expert (number of experts with a larger logit, or an
+// equal logit at a lower index); the K best write their slot.  Softmax over
+// the kept logits only (the others are -inf), shifted by the maximum.
+template <int NMAX>
+__device__ __forceinline__ void topk_gate_write(const float (&l)[NMAX], int n, int K, int t, int lane,
+                                                int32_t* topk_idx, float* topk_w, float* logits_out) {
+    float mine = 0.0f, lmax = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < NMAX; ++e) {
+        if (e < n) {
+            if (e == lane) mine = l[e];
+            lmax = fmaxf(lmax, l[e]);
+        }
+    }
+    int rank = 0;
+#pragma unroll
+    for (int e = 0; e < NMAX; ++e) {
+        if (e < n) rank += (l[e] > mine) || (l[e] == mine && e < lane);
+    }
+    const bool kept = lane < n && rank < K;
+    const float num = kept ? expf(mine - lmax) : 0.0f;
+    float z = num;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (kept) {
+        topk_idx[static_cast<size_t>(t) * K + rank] = lane;
+        topk_w[static_cast<size_t>(t) * K + rank] = num / z;
+    }
+    if (logits_out && lane < n) logits_out[static_cast<size_t>(t) * n + lane] = mine;
+}
+
+// ---------------------------------------------------------------------------
+// Router for small batches: one block of 8 warps per token.  Warp w sums the
+// 8-element chunks w, w+8, w+16, ... of the row (lane-strided), reduces them
+// with a butterfly, and warp 0 adds the 8 warp sums in warp order, so the
+// result is fixed for a given d.  All loads of a lane are issued before use.
 template <typename TX, int NMAX>
-__global__ void __launch_bounds__(512) router_topk_kernel(const TX* __restrict__ x,
+__global__ void __launch_bounds__(256) router_small_kernel(const TX* __restrict__ x, const float* __restrict__ Wg,
+                                                          const float* __restrict__ bias, int d, int n, int K,
+                                                          int32_t* __restrict__ topk_idx,
+                                                          float* __restrict__ topk_w,
+                                                          float* __restrict__ logits_out) {
+    __shared__ float part[8][NMAX];
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const TX* xr = x + static_cast<size_t>(t) * d;
+    float acc[NMAX];
+#pragma unroll
+    for (int e = 0; e < NMAX; ++e) acc[e] = 0.0f;
+    const int nchunks = d / 8;
+    for (int c0 = warp + 8 * lane; c0 < nchunks; c0 += 8 * 32 * 2) {
+        float xv[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) load8(xr, (c0 + u * 256) * 8, d, xv[u]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int j0 = (c0 + u * 256) * 8;
+            if (j0 >= d) break;
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e)
+                if (e < n) {
+                    const float* w = Wg + static_cast<size_t>(e) * d + j0;
+                    float wv[8];
+                    float4 w0 = __ldg(reinterpret_cast<const float4*>(w));
+                    float4 w1 = __ldg(reinterpret_cast<const float4*>(w + 4));
+                    wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+                    wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+                    float a = acc[e];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) a = fmaf(xv[u][q], wv[q], a);
+                    acc[e] = a;
+                }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < NMAX; ++e) {
+        if (e < n) {
+            float v = acc[e];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) part[warp][e] = v;
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float l[NMAX];
+#pragma unroll
+    for (int e = 0; e < NMAX; ++e) {
+        float v = 0.0f;
+        if (e < n) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v += part[w][e];
+            v += bias ? __ldg(bias + e) : 0.0f;
+        }
+        l[e] = v;
+    }
+    topk_gate_write<NMAX>(l, n, K, t, lane, topk_idx, topk_w, logits_out);
+}
+
+// ---------------------------------------------------------------------------
+// Router for large batches: W_g [n][d] fp32 is staged once per block in shared
+// memory, and each warp routes kTokPerWarp tokens at a time so that every
+// W_g value read from shared memory serves all of them.  Lane l owns the
+// 8-element chunks l, l+32, l+64, ... of a row and accumulates them in that
+// order; the warp adds the lanes with a butterfly, so every lane holds all n
+// logits of each token and the result does not depend on timing.
+constexpr int kTokPerWarp = 4;
+
+template <typename TX, int NMAX>
+__global__ void __launch_bounds__(256) router_topk_kernel(const TX* __restrict__ x,
                                                           const float* __restrict__ Wg,
                                                           const float* __restrict__ bias, int T,
                                                           int d, int n, int K,
@@ -25,96 +161,99 @@ __global__ void __launch_bounds__(512) router_topk_kernel(const TX* __restrict__
                                                           float* __restrict__ topk_w,
                                                           float* __restrict__ logits_out) {
     extern __shared__ float wg_s[];
-    for (int i = threadIdx.x * 4; i < n * d; i += blockDim.x * 4)
-        *reinterpret_cast<float4*>(wg_s + i) = __ldg(reinterpret_cast<const float4*>(Wg + i));
+    {
+        // stage W_g with 8 independent 16-byte loads in flight per thread
+        const int total4 = n * d / 4, stride = blockDim.x;
+        const float4* src = reinterpret_cast<const float4*>(Wg);
+        float4* dst = reinterpret_cast<float4*>(wg_s);
+        for (int i0 = threadIdx.x; i0 < total4; i0 += 8 * stride) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * stride;
+                v[u] = i < total4 ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * stride;
+                if (i < total4) dst[i] = v[u];
+            }
+        }
+    }
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
-    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
-        float acc[NMAX];
+    const int groups = (T + kTokPerWarp - 1) / kTokPerWarp;
+    for (int g = blockIdx.x * warps + (threadIdx.x >> 5); g < groups; g += gridDim.x * warps) {
+        const int t0 = g * kTokPerWarp;
+        float acc[kTokPerWarp][NMAX];
 #pragma unroll
-        for (int e = 0; e < NMAX; ++e) acc[e] = 0.0f;
-        const TX* xr = x + static_cast<size_t>(t) * d;
+        for (int q = 0; q < kTokPerWarp; ++q)
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e) acc[q][e] = 0.0f;
         for (int j0 = lane * 8; j0 < d; j0 += 256) {
-            float xv[8];
-            if constexpr (sizeof(TX) == 2) {
-                uint4 raw = __ldg(reinterpret_cast<const uint4*>(xr + j0));
-                const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw);
+            float xv[kTokPerWarp][8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) xv[u] = __bfloat162float(h[u]);
-            } else {
-                float4 a = __ldg(reinterpret_cast<const float4*>(xr + j0));
-                float4 b = __ldg(reinterpret_cast<const float4*>(xr + j0 + 4));
-                xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
-                xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+            for (int q = 0; q < kTokPerWarp; ++q) {
+                const int t = min(t0 + q, T - 1);   // tail tokens repeat the last row; not written
+                load8(x + static_cast<size_t>(t) * d, j0, d, xv[q]);
             }
 #pragma unroll
             for (int e = 0; e < NMAX; ++e) {
                 if (e < n) {
                     const float* w = wg_s + e * d + j0;
-                    float4 w0 = *reinterpret_cast<const float4*>(w);
-                    float4 w1 = *reinterpret_cast<const float4*>(w + 4);
-                    float a = acc[e];
-                    a = fmaf(xv[0], w0.x, a); a = fmaf(xv[1], w0.y, a);
-                    a = fmaf(xv[2], w0.z, a); a = fmaf(xv[3], w0.w, a);
-                    a = fmaf(xv[4], w1.x, a); a = fmaf(xv[5], w1.y, a);
-                    a = fmaf(xv[6], w1.z, a); a = fmaf(xv[7], w1.w, a);
-                    acc[e] = a;
+                    const float4 w0 = *reinterpret_cast<const float4*>(w);
+                    const float4 w1 = *reinterpret_cast<const float4*>(w + 4);
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int q = 0; q < kTokPerWarp; ++q) {
+                        float a = acc[q][e];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) a = fmaf(xv[q][u], wv[u], a);
+                        acc[q][e] = a;
+                    }
                 }
             }
         }
-        // butterfly sum: identical result in every lane
 #pragma unroll
-        for (int e = 0; e < NMAX; ++e) {
-            if (e < n) {
-                float v = acc[e];
+        for (int q = 0; q < kTokPerWarp; ++q) {
+            // butterfly sum: identical result in every lane
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                acc[e] = v + (bias ? __ldg(bias + e) : 0.0f);
+            for (int e = 0; e < NMAX; ++e) {
+                if (e < n) {
+                    float v = acc[q][e];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    acc[q][e] = v + (bias ? __ldg(bias + e) : 0.0f);
+                }
             }
+            if (t0 + q < T) topk_gate_write<NMAX>(acc[q], n, K, t0 + q, lane, topk_idx, topk_w, logits_out);
         }
-        // lane e (< n) ranks its own expert: rank = number of experts ahead of it
-        // (a larger logit, or an equal logit at a lower index).
-        float mine = 0.0f, lmax = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < NMAX; ++e) {
-            if (e < n) {
-                if (e == lane) mine = acc[e];
-                lmax = fmaxf(lmax, acc[e]);
-            }
-        }
-        int rank = 0;
-#pragma unroll
-        for (int e = 0; e < NMAX; ++e) {
-            if (e < n) rank += (acc[e] > mine) || (acc[e] == mine && e < lane);
-        }
-        const bool kept = lane < n && rank < K;
-        // Softmax over the kept logits only (the others are -inf), shifted by the max.
-        float num = kept ? expf(mine - lmax) : 0.0f;
-        float z = num;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-        if (kept) {
-            topk_idx[static_cast<size_t>(t) * K + rank] = lane;
-            topk_w[static_cast<size_t>(t) * K + rank] = num / z;
-        }
-        if (logits_out && lane < n) logits_out[static_cast<size_t>(t) * n + lane] = mine;
     }
 }
+
+// Batches up to this many tokens use the block-per-token router.
+constexpr int kSmallRouterMaxT = 512;
 
 template <typename TX, int NMAX>
 static cudaError_t launch_router_t(const void* x, const float* Wg, const float* bias, int T, int d,
                                    int n, int K, int32_t* idx, float* w, float* logits, int num_sms,
                                    cudaStream_t s) {
-    const int threads = 512, warps = threads / 32;
+    if (T <= kSmallRouterMaxT) {
+        router_small_kernel<TX, NMAX><<<T, 256, 0, s>>>(static_cast<const TX*>(x), Wg, bias, d, n, K, idx, w,
+                                                         logits);
+        return cudaGetLastError();
+    }
+    const int threads = 256, warps = threads / 32;
     const size_t smem = static_cast<size_t>(n) * d * sizeof(float);
     auto kern = router_topk_kernel<TX, NMAX>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    int blocks = (T + warps - 1) / warps;
-    if (blocks > num_sms) blocks = num_sms;
+    const int groups = (T + kTokPerWarp - 1) / kTokPerWarp;
+    int blocks = (groups + warps - 1) / warps;
+    if (blocks > 2 * num_sms) blocks = 2 * num_sms;
     if (blocks < 1) blocks = 1;
     kern<<<blocks, threads, smem, s>>>(static_cast<const TX*>(x), Wg, bias, T, d, n, K, idx, w, logits);
     return cudaGetLastError();
@@ -135,100 +274,98 @@ cudaError_t launch_router(ElemType et, const void* x, const float* Wg, const flo
 }
 
 // ---------------------------------------------------------------------------
-// Dispatch, one block of 1024 threads.  Thread i owns the contiguous run
-// [i*C, (i+1)*C) of flat assignments a = t*K + slot.  (1) per-thread expert
-// histogram; (2) exclusive scan in (expert, thread) order, which is the
-// stable order; (3) each thread scatters its run in order:
-//   perm[pos] = a, inv[a] = pos.
-// Same input -> same output, with no atomics on the data path.
+// Dispatch, one block of 1024 threads (32 warps).
+//  (1) counts[e]: shared-memory histogram of the flat assignments
+//      a = t*K + slot (the totals do not depend on the order of the adds);
+//  (2) offsets = exclusive scan of counts, and the 128-row tile prefix;
+//  (3) stable scatter, 1024 assignments per round in flat order: lanes of a
+//      warp holding the same expert find each other (match_any), a lane's rank
+//      among them is the number of such lanes below it, and the per-(warp,
+//      expert) counts are scanned across the 32 warps in warp order.  So
+//      pos = offsets[e] + (earlier rounds) + (earlier warps) + (earlier lanes):
+//      perm[pos] = a, inv[a] = pos, ascending a within every expert.
+// Same input -> same output; no atomics touch the output order.
 constexpr int kDispatchThreads = 1024;
-
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int ws = warp_sums[lane];
-        int wi = ws;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            int o = __shfl_up_sync(0xffffffffu, wi, off);
-            if (lane >= off) wi += o;
-        }
-        warp_sums[lane] = wi - ws;   // exclusive prefix of warp totals
-        if (lane == 31) warp_sums[32] = wi;
-    }
-    __syncthreads();
-    int excl = incl - v + warp_sums[warp];
-    total = warp_sums[32];
-    __syncthreads();
-    return excl;
-}
 
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int32_t* __restrict__ topk_idx,
                                                                     int R, int n, int* __restrict__ sched,
                                                                     int32_t* __restrict__ perm,
                                                                     int32_t* __restrict__ inv,
                                                                     KStatus st) {
-    extern __shared__ int hist[];   // [n][kDispatchThreads]
-    __shared__ int warp_sums[33];
+    __shared__ int s_count[32];
     __shared__ int s_off[33];
-    const int tid = threadIdx.x;
-    const int C = (R + kDispatchThreads - 1) / kDispatchThreads;
-    const int a0 = min(R, tid * C), a1 = min(R, a0 + C);
-    for (int e = 0; e < n; ++e) hist[e * kDispatchThreads + tid] = 0;
+    __shared__ int s_run[32];            // assignments of expert e placed in earlier rounds
+    __shared__ int wtab[32][33];         // [warp][expert]: count, then base, of this round
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 32) {
+        s_count[tid] = 0;
+        s_run[tid] = 0;
+    }
+    __syncthreads();
     bool bad = false;
-    for (int a = a0; a < a1; ++a) {
-        int e = topk_idx[a];
-        if (e < 0 || e >= n) { bad = true; continue; }
-        hist[e * kDispatchThreads + tid] += 1;
+    for (int a = tid; a < R; a += kDispatchThreads) {
+        const int e = topk_idx[a];
+        if (e < 0 || e >= n) {
+            bad = true;
+            continue;
+        }
+        atomicAdd(&s_count[e], 1);
     }
     if (bad) report(st, kStatusBounds);
     __syncthreads();
-    int running = 0;
-    for (int e = 0; e < n; ++e) {
-        int total;
-        int excl = block_exclusive_scan(hist[e * kDispatchThreads + tid], warp_sums, total);
-        hist[e * kDispatchThreads + tid] = excl;
-        if (tid == 0) {
-            sched[e] = total;
-            sched[n + e] = running;
-            s_off[e] = running;
-        }
-        running += total;
-    }
     if (tid == 0) {
-        sched[2 * n] = running;
-        int tp = 0;
+        int running = 0, tp = 0;
         for (int e = 0; e < n; ++e) {
+            const int c = s_count[e];
+            sched[e] = c;
+            sched[n + e] = running;
             sched[2 * n + 1 + e] = tp;
-            tp += (sched[e] + kTileM - 1) / kTileM;
+            s_off[e] = running;
+            running += c;
+            tp += (c + kTileM - 1) / kTileM;
         }
+        sched[2 * n] = running;
         sched[3 * n + 1] = tp;
     }
-    __syncthreads();
-    for (int a = a0; a < a1; ++a) {
-        int e = topk_idx[a];
-        if (e < 0 || e >= n) continue;
-        int pos = s_off[e] + hist[e * kDispatchThreads + tid]++;
-        perm[pos] = a;
-        inv[a] = pos;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < R; c0 += kDispatchThreads) {
+        const int a = c0 + tid;
+        int e = a < R ? topk_idx[a] : -1;
+        if (e >= n) e = -1;
+        wtab[warp][lane] = 0;
+        __syncwarp();
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & lt_mask);
+        if (e >= 0 && rank == 0) wtab[warp][e] = __popc(same);
+        __syncthreads();
+        if (warp < n) {
+            // warp index = expert; lane index = the warp whose count is scanned
+            const int v = wtab[lane][warp];
+            const int run = s_run[warp];
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            wtab[lane][warp] = run + incl - v;
+            __syncwarp();
+            if (lane == 31) s_run[warp] = run + incl;
+        }
+        __syncthreads();
+        if (e >= 0) {
+            const int pos = s_off[e] + wtab[warp][e] + rank;
+            perm[pos] = a;
+            inv[a] = pos;
+        }
+        __syncthreads();
     }
 }
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int R, int n, int* sched, int32_t* perm,
                             int32_t* inv, KStatus st, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(n) * kDispatchThreads * sizeof(int);
-    cudaError_t err = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    dispatch_kernel<<<1, kDispatchThreads, smem, s>>>(topk_idx, R, n, sched, perm, inv, st);
+    if (n > 32) return cudaErrorInvalidValue;
+    dispatch_kernel<<<1, kDispatchThreads, 0, s>>>(topk_idx, R, n, sched, perm, inv, st);
     return cudaGetLastError();
 }
 
@@ -242,7 +379,19 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
         const int t = perm[pos] / K;
         const uint4* src = x + static_cast<size_t>(t) * row_vecs;
         uint4* dst = Xp + static_cast<size_t>(pos) * row_vecs;
-        for (int v = lane; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+        for (int v0 = lane; v0 < row_vecs; v0 += 32 * 8) {
+            uint4 r[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < row_vecs) r[u] = __ldg(src + v);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < row_vecs) dst[v] = r[u];
+            }
+        }
     }
 }
 
