@@ -37,6 +37,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the layer is launched with
+// programmatic stream serialisation: it may start while its predecessor on the
+// stream is finishing, runs only prologue work that touches no memory another
+// kernel of the layer writes, then waits for the predecessor to complete and
+// flush (griddep_wait) before reading or writing shared buffers.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = p.n;
-    for (int i = threadIdx.x; i < 3 * n + 2; i += THREADS) s_sched[i] = p.sched[i];
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -123,6 +123,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
+    // Everything above is prologue that touches no buffer of the layer; the
+    // schedule and the activations come from the kernels before this one.
+    griddep_wait();
+    for (int i = threadIdx.x; i < 3 * n + 2; i += THREADS) s_sched[i] = p.sched[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -337,8 +341,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
     if (err != cudaSuccess) return err;
-    kern<<<num_sms, THREADS, SMEM_BYTES, s>>>(a, b0, b1, args);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(THREADS), SMEM_BYTES, s, a, b0, b1, args);
 }
 
 cudaError_t launch_tc_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1, const CUtensorMap& mapW3,

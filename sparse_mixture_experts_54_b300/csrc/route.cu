@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(256) router_small_kernel(const TX* __restrict_
                                                           float* __restrict__ topk_w,
                                                           float* __restrict__ logits_out) {
     __shared__ float part[8][NMAX];
+    griddep_launch_dependents();
+    griddep_wait();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const TX* xr = x + static_cast<size_t>(t) * d;
@@ -161,8 +163,10 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const TX* __restrict__
                                                           float* __restrict__ topk_w,
                                                           float* __restrict__ logits_out) {
     extern __shared__ float wg_s[];
+    griddep_launch_dependents();
     {
-        // stage W_g with 8 independent 16-byte loads in flight per thread
+        // Stage W_g with 8 independent 16-byte loads in flight per thread.  This
+        // prologue may overlap the previous kernel: no kernel of the layer writes W_g.
         const int total4 = n * d / 4, stride = blockDim.x;
         const float4* src = reinterpret_cast<const float4*>(Wg);
         float4* dst = reinterpret_cast<float4*>(wg_s);
@@ -180,6 +184,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const TX* __restrict__
             }
         }
     }
+    griddep_wait();
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -241,9 +246,8 @@ static cudaError_t launch_router_t(const void* x, const float* Wg, const float* 
                                    int n, int K, int32_t* idx, float* w, float* logits, int num_sms,
                                    cudaStream_t s) {
     if (T <= kSmallRouterMaxT) {
-        router_small_kernel<TX, NMAX><<<T, 256, 0, s>>>(static_cast<const TX*>(x), Wg, bias, d, n, K, idx, w,
-                                                         logits);
-        return cudaGetLastError();
+        return launch_pdl(router_small_kernel<TX, NMAX>, dim3(T), dim3(256), 0, s, static_cast<const TX*>(x), Wg,
+                          bias, d, n, K, idx, w, logits);
     }
     const int threads = 256, warps = threads / 32;
     const size_t smem = static_cast<size_t>(n) * d * sizeof(float);
@@ -255,8 +259,8 @@ static cudaError_t launch_router_t(const void* x, const float* Wg, const float* 
     int blocks = (groups + warps - 1) / warps;
     if (blocks > 2 * num_sms) blocks = 2 * num_sms;
     if (blocks < 1) blocks = 1;
-    kern<<<blocks, threads, smem, s>>>(static_cast<const TX*>(x), Wg, bias, T, d, n, K, idx, w, logits);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(blocks), dim3(threads), smem, s, static_cast<const TX*>(x), Wg, bias, T, d, n, K,
+                      idx, w, logits);
 }
 
 cudaError_t launch_router(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d,
@@ -296,6 +300,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int32_
     __shared__ int s_off[33];
     __shared__ int s_run[32];            // assignments of expert e placed in earlier rounds
     __shared__ int wtab[32][33];         // [warp][expert]: count, then base, of this round
+    griddep_launch_dependents();
+    griddep_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 32) {
         s_count[tid] = 0;
@@ -365,8 +371,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int32_
 cudaError_t launch_dispatch(const int32_t* topk_idx, int R, int n, int* sched, int32_t* perm,
                             int32_t* inv, KStatus st, cudaStream_t s) {
     if (n > 32) return cudaErrorInvalidValue;
-    dispatch_kernel<<<1, kDispatchThreads, 0, s>>>(topk_idx, R, n, sched, perm, inv, st);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_kernel, dim3(1), dim3(kDispatchThreads), 0, s, topk_idx, R, n, sched, perm, inv, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -374,6 +379,8 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int R, int n, int* sched, i
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int R,
                                                           int K, int row_vecs, uint4* __restrict__ Xp) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     for (int pos = blockIdx.x * 8 + (threadIdx.x >> 5); pos < R; pos += gridDim.x * 8) {
         const int t = perm[pos] / K;
@@ -402,9 +409,8 @@ cudaError_t launch_gather(ElemType et, const void* x, const int32_t* perm, int R
     const int row_vecs = row_bytes / 16;
     int blocks = (R + 7) / 8;
     if (blocks > 4096) blocks = 4096;
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), perm, R, K, row_vecs,
-                                              static_cast<uint4*>(Xp));
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, static_cast<const uint4*>(x), perm, R, K,
+                      row_vecs, static_cast<uint4*>(Xp));
 }
 
 // ---------------------------------------------------------------------------
@@ -413,6 +419,8 @@ cudaError_t launch_gather(ElemType et, const void* x, const int32_t* perm, int R
 template <typename TY>
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Ys, int T, int K, int d4,
                                                       TY* __restrict__ y) {
+    griddep_launch_dependents();
+    griddep_wait();
     const size_t total = static_cast<size_t>(T) * d4;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -441,12 +449,10 @@ cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, vo
     int blocks = static_cast<int>((total + 255) / 256);
     if (blocks > 148 * 16) blocks = 148 * 16;
     if (et == ElemType::BF16)
-        combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(Ys), T, K,
-                                                             d4, static_cast<__nv_bfloat16*>(y));
-    else
-        combine_kernel<float><<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(Ys), T, K, d4,
-                                                     static_cast<float*>(y));
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
+                          reinterpret_cast<const float4*>(Ys), T, K, d4, static_cast<__nv_bfloat16*>(y));
+    return launch_pdl(combine_kernel<float>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(Ys), T, K,
+                      d4, static_cast<float*>(y));
 }
 
 // ---------------------------------------------------------------------------

@@ -32,6 +32,8 @@ template <typename TX>
 __global__ void __launch_bounds__(256) simt_gemm13_kernel(const TX* __restrict__ Xp, const TX* __restrict__ W1,
                                                           const TX* __restrict__ W3, TX* __restrict__ H,
                                                           const int* __restrict__ sched, int n, int d, int F) {
+    griddep_launch_dependents();
+    griddep_wait();
     int e, row0, rend;
     if (!simt_tile(sched, n, blockIdx.x, e, row0, rend)) return;
     const int f0 = blockIdx.y * SB_N;
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(256) simt_gemm2_kernel(const TX* __restrict__ 
                                                          float* __restrict__ Ys, const int* __restrict__ sched,
                                                          const int32_t* __restrict__ perm,
                                                          const float* __restrict__ topk_w, int n, int d, int F) {
+    griddep_launch_dependents();
+    griddep_wait();
     int e, row0, rend;
     if (!simt_tile(sched, n, blockIdx.x, e, row0, rend)) return;
     const int i0 = blockIdx.y * SB_N;
@@ -142,14 +146,12 @@ cudaError_t launch_simt_gemm13(ElemType et, const void* Xp, const void* W1, cons
     if (R == 0) return cudaSuccess;
     dim3 grid(simt_max_mtiles(R, n), (F + SB_N - 1) / SB_N);
     if (et == ElemType::F32)
-        simt_gemm13_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(Xp), static_cast<const float*>(W1),
-                                                       static_cast<const float*>(W3), static_cast<float*>(H), sched,
-                                                       n, d, F);
-    else
-        simt_gemm13_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(Xp), static_cast<const __nv_bfloat16*>(W1),
-            static_cast<const __nv_bfloat16*>(W3), static_cast<__nv_bfloat16*>(H), sched, n, d, F);
-    return cudaGetLastError();
+        return launch_pdl(simt_gemm13_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(Xp),
+                          static_cast<const float*>(W1), static_cast<const float*>(W3), static_cast<float*>(H), sched,
+                          n, d, F);
+    return launch_pdl(simt_gemm13_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
+                      static_cast<const __nv_bfloat16*>(Xp), static_cast<const __nv_bfloat16*>(W1),
+                      static_cast<const __nv_bfloat16*>(W3), static_cast<__nv_bfloat16*>(H), sched, n, d, F);
 }
 
 cudaError_t launch_simt_gemm2(ElemType et, const void* H, const void* W2, float* Ys, const int* sched,
@@ -158,13 +160,10 @@ cudaError_t launch_simt_gemm2(ElemType et, const void* H, const void* W2, float*
     if (R == 0) return cudaSuccess;
     dim3 grid(simt_max_mtiles(R, n), (d + SB_N - 1) / SB_N);
     if (et == ElemType::F32)
-        simt_gemm2_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(H), static_cast<const float*>(W2), Ys,
-                                                      sched, perm, topk_w, n, d, F);
-    else
-        simt_gemm2_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(H),
-                                                              static_cast<const __nv_bfloat16*>(W2), Ys, sched,
-                                                              perm, topk_w, n, d, F);
-    return cudaGetLastError();
+        return launch_pdl(simt_gemm2_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(H),
+                          static_cast<const float*>(W2), Ys, sched, perm, topk_w, n, d, F);
+    return launch_pdl(simt_gemm2_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(H),
+                      static_cast<const __nv_bfloat16*>(W2), Ys, sched, perm, topk_w, n, d, F);
 }
 
 }  // namespace moe
