@@ -1,0 +1,459 @@
+// decode_tc.cu -- weight-streaming expert GEMMs for small batches.
+//
+// With few tokens per expert the layer reads every touched expert's weights
+// once and does little arithmetic per byte, so it is bound by HBM bandwidth,
+// not by the tensor cores (the memory-vs-compute remark of the xyznot
+// summary, "Limitations").  These kernels therefore put the weights in the
+// MMA's M operand and the expert's tokens in N ("swap-AB"):
+//
+//   MODE 0:  Da = W1_e[rows] . X_e^T,  Db = W3_e[rows] . X_e^T     (128 weight rows x N tokens)
+//   MODE 1:  D  = W2_e[rows] . H_e^T
+//
+// and split K into S parts so that (touched experts) x (row blocks) x S work
+// items spread evenly over all SMs.  Each item writes fp32 partial sums
+// P[s][row of X_e or H_e][output feature]; a small follow-up kernel adds the S
+// parts in order (then SiLU(a)*b for MODE 0, or gate, slot sum and rounding
+// for MODE 1), so results stay bitwise reproducible.
+//
+// Pipeline (one CTA per SM, persistent over its items): warp 0 lane 0 streams
+// weight tiles (128 rows x 64 K, 128-byte swizzle) and token tiles (32 rows x
+// 64 K) with TMA into a ring of stages sized to the batch; warp 1 owns tensor
+// memory and issues tcgen05.mma (M=128, N = the expert's tokens rounded up to
+// 32); warps 2-5 move finished accumulators to the partial buffers, two
+// accumulator sets in flight so the copy-out overlaps the next item.  Every
+// wait is bounded, as in gemm_tc.cu.
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int D_BK = 64;
+constexpr int D_UMMA_K = 16;
+constexpr int D_A_BYTES = 128 * D_BK * 2;   // one 128-row weight tile, 16 KB
+constexpr int D_B_BOX = 32;                 // token rows per TMA box
+constexpr int D_THREADS = 192;
+constexpr int D_EPI_THREADS = 128;
+constexpr int D_MAX_EXPERTS = 32;
+constexpr int D_MAX_STAGES = 8;
+constexpr int D_NUM_BARS = 2 * D_MAX_STAGES + 2 + 2 + 1;
+constexpr int D_TMEM_COLS = 512;
+}  // namespace
+
+struct DecArgs {
+    const int* sched;
+    int n;
+    int row_blocks;       // weight rows per expert / 128
+    int rows_per_e;       // weight rows per expert (F for MODE 0, d for MODE 1)
+    int splits;           // S
+    int kb_per_split;     // K / 64 / S
+    int n_max;            // largest token count per item, rounded up to 32 (<= 256)
+    int stages;
+    int stage_bytes;
+    int acc_stride;       // TMEM columns per accumulator set
+    int acc_sets;         // 1 or 2
+    float* Pa;            // [S][R][ld] partial sums (MODE 1: the only output)
+    float* Pb;            // [S][R][ld] (MODE 0 only)
+    int R;
+    int ld;               // output features (F for MODE 0, d for MODE 1)
+    KStatus st;
+};
+
+static size_t decode_smem_bytes(int stages, int stage_bytes) {
+    return 1024 + static_cast<size_t>(stages) * stage_bytes + D_NUM_BARS * 8 + 16 + (3 * D_MAX_EXPERTS + 2) * 4 +
+           D_MAX_EXPERTS * 4;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(D_THREADS, 1)
+    tc_decode_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB, DecArgs p) {
+    constexpr int A_TILES = MODE == 0 ? 2 : 1;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* ring_ptr = smem_raw + (ring_u32 - raw_u32);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + static_cast<size_t>(p.stages) * p.stage_bytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + D_NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_sched = reinterpret_cast<int*>(tmem_slot + 4);
+    int* s_touched = s_sched + 3 * D_MAX_EXPERTS + 2;   // touched experts, in expert order
+
+    const uint32_t bar0 = smem_u32(bars);
+    const int S = p.stages;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (D_MAX_STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * D_MAX_STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * D_MAX_STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * D_MAX_STAGES + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = p.n;
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), D_EPI_THREADS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA0);
+        if (MODE == 0) tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), D_TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Everything above touches no buffer of the layer; the schedule and the
+    // token rows come from the kernels before this one.
+    griddep_wait();
+    for (int i = threadIdx.x; i < 3 * n + 2; i += D_THREADS) s_sched[i] = p.sched[i];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0) {
+        int nt = 0;
+        for (int e = 0; e < n; ++e)
+            if (s_sched[e] > 0) s_touched[nt++] = e;
+        s_touched[D_MAX_EXPERTS - 1] = nt;   // count kept in the last slot (n <= 31)
+    }
+    __syncthreads();
+    const uint32_t tmem_base = *tmem_slot;
+    const int* counts = s_sched;
+    const int* offsets = s_sched + n;
+    const int n_touched = s_touched[D_MAX_EXPERTS - 1];
+    const int items = n_touched * p.row_blocks * p.splits;
+    const KStatus st = p.st;
+
+    // item -> (expert, weight row block, K split); K split varies fastest
+    auto decode_item = [&](int it, int& e, int& rb, int& sp) {
+        sp = it % p.splits;
+        const int r = it / p.splits;
+        rb = r % p.row_blocks;
+        e = s_touched[r / p.row_blocks];
+    };
+    auto item_n = [&](int e) {
+        const int c = counts[e];
+        const int nn = (c + D_B_BOX - 1) / D_B_BOX * D_B_BOX;
+        return nn < D_B_BOX ? D_B_BOX : nn;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            const uint64_t pol_w = policy_evict_first();   // each weight byte is read once
+            const uint64_t pol_x = policy_evict_last();    // token rows are re-read by every row block
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                int e, rb, sp;
+                decode_item(it, e, rb, sp);
+                const int nbox = item_n(e) / D_B_BOX;
+                const int arow = e * p.rows_per_e + rb * 128;
+                const int brow = offsets[e];
+                const uint32_t bytes = A_TILES * D_A_BYTES + nbox * D_B_BOX * D_BK * 2;
+                for (int kb = sp * p.kb_per_split; kb < (sp + 1) * p.kb_per_split; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
+                    const uint32_t a_dst = ring_u32 + stage * p.stage_bytes;
+                    const uint32_t b_dst = a_dst + A_TILES * D_A_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    tma_load_2d(a_dst, &tmA0, full_bar(stage), kb * D_BK, arow, pol_w);
+                    if (MODE == 0) tma_load_2d(a_dst + D_A_BYTES, &tmA1, full_bar(stage), kb * D_BK, arow, pol_w);
+                    for (int bb = 0; bb < nbox; ++bb)
+                        tma_load_2d(b_dst + bb * D_B_BOX * D_BK * 2, &tmB, full_bar(stage), kb * D_BK,
+                                    brow + bb * D_B_BOX, pol_x);
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                report(st, kStatusTimeout);
+                *abort_flag = 1;
+            }
+            if (*abort_flag) {
+                // every stage's most recent load must land before the CTA exits
+                for (int s = 0; s < S; ++s) {
+                    if (issued <= s) continue;
+                    const long long last = issued - 1 - ((issued - 1 - s) % S);
+                    mbar_wait(full_bar(s), static_cast<uint32_t>((last / S) & 1), st, nullptr);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                int e, rb, sp;
+                decode_item(it, e, rb, sp);
+                const int N = item_n(e);
+                const uint32_t idesc = idesc_bf16_f32(128, N);
+                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, st, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * p.acc_stride);
+                const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
+                for (int k = 0; k < p.kb_per_split; ++k) {
+                    if (!mbar_wait(full_bar(stage), phase, st, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = ring_u32 + stage * p.stage_bytes;
+                    const uint64_t adesc0 = sdesc_kmajor_sw128(a_addr);
+                    const uint64_t adesc1 = sdesc_kmajor_sw128(a_addr + D_A_BYTES);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + A_TILES * D_A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < D_BK / D_UMMA_K; ++kk) {
+                        const uint32_t accum = (k | kk) != 0;
+                        mma_bf16_ss(d0, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, accum);
+                        if (MODE == 0) mma_bf16_ss(d1, adesc1 + 2u * kk, bdesc + 2u * kk, idesc, accum);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(accf_bar(acc));
+                if (++acc == p.acc_sets) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                report(st, kStatusTimeout);
+                *abort_flag = 1;
+            }
+            mma_commit(drain_bar);
+            if (!mbar_wait(drain_bar, 0, st, nullptr)) report(st, kStatusTimeout);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: accumulator -> fp32 partial sums ----------------
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items; it += gridDim.x) {
+            int e, rb, sp;
+            decode_item(it, e, rb, sp);
+            const int N = item_n(e);
+            const int cnt = counts[e];
+            const int off = offsets[e];
+            if (!mbar_wait(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const int feat = rb * 128 + q * 32 + lane;   // this thread's weight row = output feature
+            const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+            const uint32_t t0 = tmem_base + static_cast<uint32_t>(acc * p.acc_stride) + lane_off;
+            for (int part = 0; part < A_TILES; ++part) {
+                float* P = (part == 0 ? p.Pa : p.Pb) + static_cast<size_t>(sp) * p.R * p.ld;
+                const uint32_t tp = t0 + static_cast<uint32_t>(part * p.n_max);
+                for (int c = 0; c < N; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tp + c, v);
+                    tmem_ld_wait();
+                    const int jn = min(32, cnt - c);
+                    float* dst = P + static_cast<size_t>(off + c) * p.ld + feat;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) dst[static_cast<size_t>(j) * p.ld] = __uint_as_float(v[j]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acce_bar(acc));
+            if (++acc == p.acc_sets) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (!ok) {
+            if (lane == 0) report(st, kStatusTimeout);
+            *abort_flag = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, D_TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// H[r][f] = bf16( SiLU(sum_s Pa[s][r][f]) * sum_s Pb[s][r][f] ), parts added in order.
+__global__ void __launch_bounds__(256) decode_swiglu_kernel(const float4* __restrict__ Pa, const float4* __restrict__ Pb,
+                                                            int S, size_t part4, uint2* __restrict__ H) {
+    griddep_launch_dependents();
+    griddep_wait();
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < part4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float4 a = __ldg(Pa + i), b = __ldg(Pb + i);
+        for (int s = 1; s < S; ++s) {
+            const float4 a2 = __ldg(Pa + s * part4 + i), b2 = __ldg(Pb + s * part4 + i);
+            a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+            b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+        }
+        uint2 o;
+        o.x = pack_bf16x2(silu_f(a.x) * b.x, silu_f(a.y) * b.y);
+        o.y = pack_bf16x2(silu_f(a.z) * b.z, silu_f(a.w) * b.w);
+        H[i] = o;
+    }
+}
+
+// y[t][i] = sum_k g[t][k] * (sum_s P2[s][inv[t*K+k]][i]), slots in order, one rounding.
+template <typename TY>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __restrict__ P2, int S, size_t part4,
+                                                             const int32_t* __restrict__ inv,
+                                                             const float* __restrict__ topk_w, int T, int K, int d4,
+                                                             TY* __restrict__ y) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const size_t total = static_cast<size_t>(T) * d4;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t t = i / d4, c = i % d4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+            const size_t a = t * K + k;
+            const size_t row = static_cast<size_t>(inv[a]);
+            const float g = topk_w[a];
+            float4 v = __ldg(P2 + row * d4 + c);
+            for (int s = 1; s < S; ++s) {
+                const float4 v2 = __ldg(P2 + s * part4 + row * d4 + c);
+                v.x += v2.x; v.y += v2.y; v.z += v2.z; v.w += v2.w;
+            }
+            acc.x += g * v.x; acc.y += g * v.y; acc.z += g * v.z; acc.w += g * v.w;
+        }
+        if constexpr (sizeof(TY) == 4) {
+            reinterpret_cast<float4*>(y)[i] = acc;
+        } else {
+            uint2 o;
+            o.x = pack_bf16x2(acc.x, acc.y);
+            o.y = pack_bf16x2(acc.z, acc.w);
+            reinterpret_cast<uint2*>(y)[i] = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+// Number of K splits for `units` (expert, row block) pairs: the smallest divisor
+// of kblocks (<= kDecodeMaxSplits) whose items fill the SMs' waves to >= 95%,
+// else the one that fills them best.
+int decode_pick_splits(int units, int kblocks, int num_sms) {
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= kDecodeMaxSplits; ++s) {
+        if (kblocks % s) continue;
+        const long long items = static_cast<long long>(units) * s;
+        const long long waves = (items + num_sms - 1) / num_sms;
+        const double eff = static_cast<double>(items) / static_cast<double>(waves * num_sms);
+        if (eff >= 0.95) return s;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+static bool decode_layout(int mode, int n_max, int& stages, int& stage_bytes, int& acc_stride, int& acc_sets) {
+    const int a_tiles = mode == 0 ? 2 : 1;
+    stage_bytes = a_tiles * D_A_BYTES + n_max * D_BK * 2;
+    stages = static_cast<int>((200 * 1024) / stage_bytes);
+    if (stages > D_MAX_STAGES) stages = D_MAX_STAGES;
+    if (stages < 2) return false;
+    acc_stride = a_tiles * n_max;
+    acc_sets = (2 * acc_stride <= D_TMEM_COLS) ? 2 : 1;
+    return acc_stride <= D_TMEM_COLS;
+}
+
+template <int MODE>
+static cudaError_t launch_decode(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, DecArgs args,
+                                 int num_sms, cudaStream_t s) {
+    if (!decode_layout(MODE, args.n_max, args.stages, args.stage_bytes, args.acc_stride, args.acc_sets))
+        return cudaErrorInvalidValue;
+    const size_t smem = decode_smem_bytes(args.stages, args.stage_bytes);
+    auto kern = tc_decode_kernel<MODE>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(num_sms), dim3(D_THREADS), smem, s, a0, a1, b, args);
+}
+
+cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
+                              const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,
+                              KStatus st, int num_sms, cudaStream_t s) {
+    if (n > D_MAX_EXPERTS - 1 || T <= 0 || T > kDecodeMaxT) return cudaErrorInvalidValue;
+    DecArgs args{};
+    args.sched = sched;
+    args.n = n;
+    args.row_blocks = F / 128;
+    args.rows_per_e = F;
+    args.splits = splits;
+    args.kb_per_split = d / D_BK / splits;
+    args.n_max = (T + D_B_BOX - 1) / D_B_BOX * D_B_BOX;
+    args.Pa = Pa;
+    args.Pb = Pb;
+    args.R = K * T;
+    args.ld = F;
+    args.st = st;
+    return launch_decode<0>(mapW1, mapW3, mapXp32, args, num_sms, s);
+}
+
+cudaError_t launch_decode_w2(const CUtensorMap& mapW2, const CUtensorMap& mapH32, const int* sched, int n, int d,
+                             int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s) {
+    if (n > D_MAX_EXPERTS - 1 || T <= 0 || T > kDecodeMaxT) return cudaErrorInvalidValue;
+    DecArgs args{};
+    args.sched = sched;
+    args.n = n;
+    args.row_blocks = d / 128;
+    args.rows_per_e = d;
+    args.splits = splits;
+    args.kb_per_split = F / D_BK / splits;
+    args.n_max = (T + D_B_BOX - 1) / D_B_BOX * D_B_BOX;
+    args.Pa = P2;
+    args.Pb = nullptr;
+    args.R = K * T;
+    args.ld = d;
+    args.st = st;
+    return launch_decode<1>(mapW2, mapW2, mapH32, args, num_sms, s);
+}
+
+cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R, int F, __nv_bfloat16* H,
+                                 cudaStream_t s) {
+    const size_t part4 = static_cast<size_t>(R) * F / 4;
+    int blocks = static_cast<int>((part4 + 255) / 256);
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(decode_swiglu_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(Pa),
+                      reinterpret_cast<const float4*>(Pb), S, part4, reinterpret_cast<uint2*>(H));
+}
+
+cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
+                                  int T, int K, int d, void* y, cudaStream_t s) {
+    const size_t part4 = static_cast<size_t>(R) * d / 4;
+    const int d4 = d / 4;
+    const size_t total = static_cast<size_t>(T) * d4;
+    int blocks = static_cast<int>((total + 255) / 256);
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks < 1) blocks = 1;
+    if (et == ElemType::BF16)
+        return launch_pdl(decode_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
+                          reinterpret_cast<const float4*>(P2), S, part4, inv, topk_w, T, K, d4,
+                          static_cast<__nv_bfloat16*>(y));
+    return launch_pdl(decode_combine_kernel<float>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2),
+                      S, part4, inv, topk_w, T, K, d4, static_cast<float*>(y));
+}
+
+}  // namespace moe

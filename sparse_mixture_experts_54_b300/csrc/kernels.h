@@ -64,6 +64,20 @@ cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, c
                             int d, int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
                             KStatus st, int num_sms, cudaStream_t s);
 
+// weight-streaming decode path (bf16, small T) ----------------------------------
+constexpr int kDecodeMaxT = 256;     // tokens per call the decode kernels accept
+constexpr int kDecodeMaxSplits = 16;
+int decode_pick_splits(int units, int kblocks, int num_sms);
+cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
+                              const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,
+                              KStatus st, int num_sms, cudaStream_t s);
+cudaError_t launch_decode_w2(const CUtensorMap& mapW2_128, const CUtensorMap& mapH32, const int* sched, int n, int d,
+                             int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s);
+cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R, int F, __nv_bfloat16* H,
+                                 cudaStream_t s);
+cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
+                                  int T, int K, int d, void* y, cudaStream_t s);
+
 // self-test of the bounded waits -------------------------------------------------
 cudaError_t launch_wait_selftest(KStatus st, cudaStream_t s);
 

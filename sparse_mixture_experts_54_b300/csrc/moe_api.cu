@@ -15,7 +15,7 @@ struct moe_ctx {
     int d = 0, F = 0, n = 0, k = 0;
     int dtype = MOE_BF16;
     const float* bias = nullptr;
-    int decode_max_t = 0;
+    int decode_max_t = 64;
     long long wait_limit_us = 2000000;
     int force_path = 0;
     int device = 0;
@@ -24,6 +24,7 @@ struct moe_ctx {
     int* status_dev = nullptr;    // device alias
     // workspace (one allocation)
     int cap_T = -1;
+    int cap_dec = 0;            // tokens the decode partial-sum buffers hold
     void* ws = nullptr;
     size_t ws_bytes = 0;
     int32_t* topk_idx = nullptr;
@@ -36,7 +37,10 @@ struct moe_ctx {
     float* Ys = nullptr;
     void* xbuf = nullptr;
     void* ybuf = nullptr;
-    CUtensorMap map_Xp, map_H;
+    float* Pa = nullptr;        // decode partial sums [S][R][F] (W1 rows), [S][R][F] (W3 rows)
+    float* Pb = nullptr;
+    float* P2 = nullptr;        // decode partial sums [S][R][d] (W2 rows)
+    CUtensorMap map_Xp, map_H, map_Xp32, map_H32;
     bool maps_ok = false;
     // per-stage CUDA-event timing (MOE_OPT_STAGE_TIMING)
     bool stage_timing = false;
@@ -50,10 +54,10 @@ size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t topk_idx, topk_w, perm, inv, sched, Xp, H, Ys, xbuf, ybuf, total;
+    size_t topk_idx, topk_w, perm, inv, sched, Xp, H, Ys, xbuf, ybuf, Pa, Pb, P2, total;
 };
 
-Layout layout_for(const moe_ctx* c, int T) {
+Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     Layout L{};
     const size_t R = static_cast<size_t>(c->k) * static_cast<size_t>(T > 0 ? T : 1);
     const size_t Tn = static_cast<size_t>(T > 0 ? T : 1);
@@ -70,6 +74,10 @@ Layout layout_for(const moe_ctx* c, int T) {
     L.Ys = take(R * c->d * 4);
     L.xbuf = take(Tn * c->d * es);
     L.ybuf = take(Tn * c->d * es);
+    const size_t Rd = static_cast<size_t>(c->k) * static_cast<size_t>(Tdec > 0 ? Tdec : 0);
+    L.Pa = take(kDecodeMaxSplits * Rd * c->F * 4);
+    L.Pb = take(kDecodeMaxSplits * Rd * c->F * 4);
+    L.P2 = take(kDecodeMaxSplits * Rd * c->d * 4);
     L.total = off;
     return L;
 }
@@ -90,20 +98,26 @@ bool env_flag(const char* name) {
     return v && *v && strcmp(v, "0") != 0;
 }
 
-// Make sure the workspace holds T tokens.  Growth frees the old buffer after
-// synchronising the stream; it is refused while the stream is being captured.
-int ensure_workspace(moe_ctx* c, int T, cudaStream_t s) {
-    if (T <= c->cap_T && c->ws) return MOE_OK;
+// Make sure the workspace holds T tokens (and, for the decode kernels, their
+// partial sums).  Growth frees the old buffer after synchronising the stream;
+// it is refused while the stream is being captured.
+int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
+    if (T <= c->cap_T && c->ws && (!decode || T <= c->cap_dec)) return MOE_OK;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) return MOE_ERR_INVALID;
     if (env_flag("MOE_FAIL_WORKSPACE_ALLOC")) return MOE_ERR_OOM;   // host-side fault injection for tests
-    Layout L = layout_for(c, T);
+    int Tdec = decode ? T : 0;
+    if (Tdec > kDecodeMaxT) Tdec = kDecodeMaxT;
+    if (c->ws && c->cap_dec > Tdec) Tdec = c->cap_dec;
+    if (c->ws && c->cap_T > T) T = c->cap_T;
+    Layout L = layout_for(c, T, Tdec);
     if (c->ws) {
         cudaStreamSynchronize(s);
         cudaDeviceSynchronize();
         cudaFree(c->ws);
         c->ws = nullptr;
         c->cap_T = -1;
+        c->cap_dec = 0;
         c->maps_ok = false;
     }
     void* p = nullptr;
@@ -125,19 +139,31 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s) {
     c->Ys = reinterpret_cast<float*>(b + L.Ys);
     c->xbuf = b + L.xbuf;
     c->ybuf = b + L.ybuf;
+    c->Pa = reinterpret_cast<float*>(b + L.Pa);
+    c->Pb = reinterpret_cast<float*>(b + L.Pb);
+    c->P2 = reinterpret_cast<float*>(b + L.P2);
     c->cap_T = T;
+    c->cap_dec = Tdec;
     // Tensor maps of the workspace activations cover the full capacity; rows
     // beyond the live K*T are never valid rows of any tile.
     if (c->dtype == MOE_BF16) {
         const uint64_t R = static_cast<uint64_t>(c->k) * static_cast<uint64_t>(T > 0 ? T : 1);
         c->maps_ok = encode_map_bf16_2d(&c->map_Xp, c->Xp, R, c->d, 128) &&
-                     encode_map_bf16_2d(&c->map_H, c->H, R, c->F, 128);
+                     encode_map_bf16_2d(&c->map_H, c->H, R, c->F, 128) &&
+                     encode_map_bf16_2d(&c->map_Xp32, c->Xp, R, c->d, 32) &&
+                     encode_map_bf16_2d(&c->map_H32, c->H, R, c->F, 32);
         if (!c->maps_ok) return MOE_ERR_CUDA;
     }
     return MOE_OK;
 }
 
 bool tc_shape_ok(const moe_ctx* c) { return c->d % 256 == 0 && c->F % 128 == 0; }
+
+// The weight-streaming kernels serve bf16 batches of up to decode_max_t tokens.
+bool use_decode(const moe_ctx* c, int T) {
+    if (c->dtype != MOE_BF16 || c->n > 31 || T > kDecodeMaxT || c->force_path == 1) return false;
+    return c->force_path == 2 || T <= c->decode_max_t;
+}
 
 // Stages of one forward call, in launch order.
 constexpr int kStages = 6;
@@ -213,6 +239,30 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         e = launch_simt_gemm2(et, c->H, W2, c->Ys, c->sched, c->perm, c->topk_w, c->n, c->d, c->F, R, s);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.mark(4);
+    } else if (use_decode(c, T)) {
+        CUtensorMap mW1, mW3, mW2;
+        const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
+        if (!encode_map_bf16_2d(&mW1, W1, nF, c->d, 128) || !encode_map_bf16_2d(&mW3, W3, nF, c->d, 128) ||
+            !encode_map_bf16_2d(&mW2, W2, nd, c->F, 128))
+            return MOE_ERR_CUDA;
+        const KStatus st = kstatus(c);
+        const int touched = c->n < R ? c->n : R;
+        const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 64, c->num_sms);
+        const int s1 = decode_pick_splits(touched * (c->d / 128), c->F / 64, c->num_sms);
+        e = launch_decode_w13(mW1, mW3, c->map_Xp32, c->sched, c->n, c->d, c->F, T, c->k, s0, c->Pa, c->Pb, st,
+                              c->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(3);
+        e = launch_decode_w2(mW2, c->map_H32, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(4);
+        e = launch_decode_combine(et, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, y, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.mark(5);
+        marks.finish();
+        return MOE_OK;
     } else {
         CUtensorMap mW1, mW3, mW2;
         const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
@@ -277,6 +327,7 @@ int moe_set_dtype(moe_ctx* c, int dtype) {
             cudaFree(c->ws);
             c->ws = nullptr;
             c->cap_T = -1;
+            c->cap_dec = 0;
             c->maps_ok = false;
         }
         c->dtype = dtype;
@@ -317,12 +368,18 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
 
 size_t moe_workspace_bytes(const moe_ctx* c, int T) {
     if (!c || T < 0) return 0;
-    return layout_for(c, T).total;
+    int Tdec = T < c->decode_max_t ? T : c->decode_max_t;
+    if (Tdec > kDecodeMaxT) Tdec = kDecodeMaxT;
+    return layout_for(c, T, c->dtype == MOE_BF16 ? Tdec : 0).total;
 }
 
 int moe_reserve(moe_ctx* c, int T_max) {
     if (!c || T_max < 0) return MOE_ERR_INVALID;
-    return ensure_workspace(c, T_max, nullptr);
+    int Tdec = T_max < c->decode_max_t ? T_max : c->decode_max_t;
+    if (Tdec > kDecodeMaxT) Tdec = kDecodeMaxT;
+    int rc = ensure_workspace(c, T_max, nullptr, false);
+    if (rc == MOE_OK && c->dtype == MOE_BF16 && Tdec > 0) rc = ensure_workspace(c, Tdec, nullptr, true);
+    return rc;
 }
 
 int moe_route(moe_ctx* c, const void* x, const float* Wg, int T, int32_t* topk_idx, float* topk_w, int32_t* counts,
@@ -371,7 +428,7 @@ int moe_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         return MOE_ERR_INVALID;
     if (c->dtype == MOE_BF16 && !tc_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int rc = ensure_workspace(c, T, s);
+    int rc = ensure_workspace(c, T, s, use_decode(c, T));
     if (rc != MOE_OK) return rc;
     return run_forward(c, x, Wg, W1, W3, W2, y, T, s);
 }
@@ -384,7 +441,7 @@ int moe_forward_host(moe_ctx* c, const void* x_host, const float* Wg, const void
     if (!Wg || !W1 || !W3 || !W2) return MOE_ERR_INVALID;
     if (c->dtype == MOE_BF16 && !tc_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int rc = ensure_workspace(c, T, s);
+    int rc = ensure_workspace(c, T, s, use_decode(c, T));
     if (rc != MOE_OK) return rc;
     const size_t bytes = static_cast<size_t>(T) * c->d * esize(c->dtype);
     if (cudaMemcpyAsync(c->xbuf, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -149,3 +149,52 @@ def test_mixtral_prefill_t4096_sampled(mixtral_experts):
 
 def test_mixtral_skewed_t32768_sampled(mixtral_experts):
     _mixtral_case("skewed_t32768", mixtral_experts, 48)
+
+
+# ----------------------------------------------------------------------------- decode (weight-streaming) path
+DECODE_CASES = [
+    # T, d, F, n, K
+    (1, 256, 256, 8, 2),
+    (5, 512, 384, 8, 2),
+    (32, 256, 256, 8, 2),
+    (64, 512, 256, 8, 2),
+    (200, 512, 384, 8, 2),
+    (100, 256, 256, 4, 1),
+    (77, 256, 384, 8, 3),
+    (120, 768, 640, 16, 2),
+    (256, 256, 256, 8, 2),
+]
+
+
+@pytest.mark.parametrize("T,d,F,n,K", DECODE_CASES)
+def test_decode_path_matches_oracle(T, d, F, n, K):
+    w = inputs.Workload("dec", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=100 + T + d)
+    layer = inputs.make_layer(w, "cuda")
+    m, y, gidx, gw = run_layer(w, layer, path=2)
+    y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
+    check_route(gidx, gw, ref["logits"], ref["idx"], ref["gate"], K)
+    assert_close(y_to_numpy(y), y_ref, "bf16")
+
+
+def test_decode_all_tokens_to_one_expert_pair():
+    # 200 tokens on experts (5, 2): N = 224 token columns per item, other experts skipped
+    w = inputs.Workload("dec_skew", T=200, d=256, d_ff=384, bias=(0, 0, 50, 0, 0, 100, 0, 0), seed=4)
+    layer = inputs.make_layer(w, "cuda")
+    m, y, gidx, gw = run_layer(w, layer, path=2)
+    assert np.all(gidx == [5, 2])
+    y_ref, ref, near = oracle_y(layer, w, np.arange(w.T), gidx)
+    assert_close(y_to_numpy(y), y_ref, "bf16")
+
+
+def test_decode_and_grouped_paths_agree_and_are_deterministic():
+    w = inputs.Workload("dec_vs_grp", T=48, d=512, d_ff=384, seed=9)
+    layer = inputs.make_layer(w, "cuda")
+    _, y_dec, _, _ = run_layer(w, layer, path=2)
+    _, y_dec2, _, _ = run_layer(w, layer, path=2)
+    _, y_grp, _, _ = run_layer(w, layer, path=1)
+    assert torch.equal(y_dec, y_dec2)
+    assert_close(y_to_numpy(y_dec), y_to_numpy(y_grp), "bf16")
+
+
+def test_mixtral_decode_t32_grouped_path(mixtral_experts):
+    _mixtral_case("decode_t32", mixtral_experts, 32, path=1)
