@@ -64,6 +64,15 @@ cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, c
                             int d, int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
                             KStatus st, int num_sms, cudaStream_t s);
 
+// tcgen05 grouped GEMMs on CTA pairs (cta_group::2; 256-row tiles) -------------
+bool pair_gemm_available(int num_sms);
+cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1, const CUtensorMap& mapW3,
+                               const int* sched, int n, int d, int F, int R, __nv_bfloat16* H, KStatus st,
+                               int num_sms, cudaStream_t s);
+cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_128, const int* sched, int n, int d,
+                              int F, int R, float* Ys, const int32_t* perm, const float* topk_w, KStatus st,
+                              int num_sms, cudaStream_t s);
+
 // weight-streaming decode path (bf16, small T) ----------------------------------
 constexpr int kDecodeMaxT = 256;     // tokens per call the decode kernels accept
 constexpr int kDecodeMaxSplits = 16;

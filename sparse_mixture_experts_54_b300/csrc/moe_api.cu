@@ -18,6 +18,7 @@ struct moe_ctx {
     int decode_max_t = 64;
     long long wait_limit_us = 2000000;
     int force_path = 0;
+    int gemm_pair = 0;          // 0 auto, 1 single CTA, 2 CTA pairs
     int device = 0;
     int num_sms = 148;
     int* status_host = nullptr;   // host-mapped
@@ -165,6 +166,16 @@ bool use_decode(const moe_ctx* c, int T) {
     return c->force_path == 2 || T <= c->decode_max_t;
 }
 
+// The grouped GEMMs run on single CTAs (128-row tiles) unless the caller asks
+// for CTA pairs.  Pairs move a third fewer operand bytes per FLOP and take ~10%
+// fewer cycles per launch, but their 256-row tiles pad each expert group by
+// 128 rows on average, and under the board's power cap that extra tensor work
+// costs more clock than the saved traffic gives back (measured at T=4096).
+bool use_pair(const moe_ctx* c) {
+    if (c->gemm_pair != 2) return false;
+    return pair_gemm_available(c->num_sms);
+}
+
 // Stages of one forward call, in launch order.
 constexpr int kStages = 6;
 const char* const kStageNames[kStages] = {"router", "dispatch", "gather", "expert_w1w3_swiglu",
@@ -264,18 +275,28 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         marks.finish();
         return MOE_OK;
     } else {
+        const bool pair = use_pair(c);
+        if (c->gemm_pair == 2 && !pair) return MOE_ERR_UNSUPPORTED;
         CUtensorMap mW1, mW3, mW2;
         const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
         if (!encode_map_bf16_2d(&mW1, W1, nF, c->d, 128) || !encode_map_bf16_2d(&mW3, W3, nF, c->d, 128) ||
-            !encode_map_bf16_2d(&mW2, W2, nd, c->F, 256))
+            !encode_map_bf16_2d(&mW2, W2, nd, c->F, pair ? 128 : 256))
             return MOE_ERR_CUDA;
         const KStatus st = kstatus(c);
-        e = launch_tc_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
-                             static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
+        if (pair)
+            e = launch_pair_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
+                                   static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
+        else
+            e = launch_tc_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
+                                 static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.mark(3);
-        e = launch_tc_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, st,
-                            c->num_sms, s);
+        if (pair)
+            e = launch_pair_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, st,
+                                  c->num_sms, s);
+        else
+            e = launch_tc_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, st,
+                                c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.mark(4);
     }
@@ -356,6 +377,10 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
         case MOE_OPT_FORCE_PATH:
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
             c->force_path = static_cast<int>(value);
+            return MOE_OK;
+        case MOE_OPT_GEMM_PAIR:
+            if (value < 0 || value > 2) return MOE_ERR_INVALID;
+            c->gemm_pair = static_cast<int>(value);
             return MOE_OK;
         case MOE_OPT_STAGE_TIMING:
             if (value < 0 || value > 1) return MOE_ERR_INVALID;

@@ -21,10 +21,12 @@ def oracle_y(layer, w, toks, gpu_idx):
     return y, ref, near
 
 
-def run_layer(w, layer, path=0):
+def run_layer(w, layer, path=0, pair=0):
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, dtype=w.torch_dtype, bias=layer["bias"])
     if path:
         m.set_option(_lib.MOE_OPT_FORCE_PATH, path)
+    if pair:
+        m.set_option(_lib.MOE_OPT_GEMM_PAIR, pair)
     r = m.route(layer["x"], layer["Wg"])
     y = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
     torch.cuda.synchronize()
@@ -55,24 +57,55 @@ SMALL_BF16 = [
 ]
 
 
+# grouped GEMM kernels: 1 = single CTA (128-row tiles), 2 = CTA pairs (256-row tiles)
+GEMM_KINDS = [1, 2]
+
+
+@pytest.mark.parametrize("pair", GEMM_KINDS)
 @pytest.mark.parametrize("T,d,F,n,K", SMALL_BF16)
-def test_bf16_small_shapes(T, d, F, n, K):
+def test_bf16_small_shapes(T, d, F, n, K, pair):
     w = inputs.Workload("small", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=T + d)
     layer = inputs.make_layer(w, "cuda")
-    m, y, gidx, gw = run_layer(w, layer)
+    m, y, gidx, gw = run_layer(w, layer, path=1, pair=pair)
     y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
     check_route(gidx, gw, ref["logits"], ref["idx"], ref["gate"], K)
     assert_close(y_to_numpy(y), y_ref, "bf16")
 
 
-def test_bf16_all_tokens_one_expert_pair():
-    # every token to experts (5, 2): one group of 700 rows (6 tiles, ragged), all other experts empty
+@pytest.mark.parametrize("pair", GEMM_KINDS)
+def test_bf16_all_tokens_one_expert_pair(pair):
+    # every token to experts (5, 2): two groups of 700 rows (6 single-CTA tiles or
+    # 3 pair tiles each, ragged), all other experts empty
     w = inputs.Workload("skew", T=700, d=256, d_ff=256, bias=(0, 0, 50, 0, 0, 100, 0, 0), seed=3)
     layer = inputs.make_layer(w, "cuda")
-    m, y, gidx, gw = run_layer(w, layer)
+    m, y, gidx, gw = run_layer(w, layer, path=1, pair=pair)
     assert np.all(gidx == [5, 2])
     y_ref, ref, near = oracle_y(layer, w, np.arange(w.T), gidx)
     assert_close(y_to_numpy(y), y_ref, "bf16")
+
+
+@pytest.mark.parametrize("T", [128, 129, 256, 257, 384, 513])
+def test_pair_tile_boundaries(T):
+    # K=1 with every token on expert 3: one group of exactly T rows, so the pair
+    # tiles end on, just past and inside a 128/256-row boundary
+    w = inputs.Workload("edge", T=T, d=256, d_ff=384, k=1, bias=(0, 0, 0, 80, 0, 0, 0, 0), seed=T)
+    layer = inputs.make_layer(w, "cuda")
+    _, y1, gidx, _ = run_layer(w, layer, path=1, pair=1)
+    _, y2, _, _ = run_layer(w, layer, path=1, pair=2)
+    assert np.all(gidx[:, 0] == 3)
+    y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
+    assert_close(y_to_numpy(y2), y_ref, "bf16")
+    assert_close(y_to_numpy(y1), y_ref, "bf16")
+
+
+def test_pair_and_single_cta_agree_and_are_deterministic():
+    w = inputs.Workload("pair_vs_single", T=1500, d=512, d_ff=640, seed=21)
+    layer = inputs.make_layer(w, "cuda")
+    _, y1, _, _ = run_layer(w, layer, path=1, pair=1)
+    _, y2, _, _ = run_layer(w, layer, path=1, pair=2)
+    _, y3, _, _ = run_layer(w, layer, path=1, pair=2)
+    assert torch.equal(y2, y3)
+    assert_close(y_to_numpy(y2), y_to_numpy(y1).astype(np.float64), "bf16")
 
 
 def test_bf16_fp32_fallback_shape_rejected():
@@ -120,13 +153,13 @@ def mixtral_experts():
     return (W1, W3, W2), host
 
 
-def _mixtral_case(name, mixtral_experts, sample, path=0):
+def _mixtral_case(name, mixtral_experts, sample, path=0, pair=0):
     w = inputs.workload(name)
     (W1, W3, W2), (h1, h3, h2) = mixtral_experts
     x = inputs.make_x(w, "cuda")
     Wg, b = inputs.make_router(w, "cuda")
     layer = dict(x=x, Wg=Wg, bias=b, W1=W1, W3=W3, W2=W2)
-    m, y, gidx, gw = run_layer(w, layer, path)
+    m, y, gidx, gw = run_layer(w, layer, path, pair)
     toks = inputs.sample_tokens(w.T, sample).numpy()
     xo, Wgo, bo = inputs.to_oracle(x), inputs.to_oracle(Wg), inputs.to_oracle(b)
     logits = oracle.router_logits(xo, Wgo, bo)
@@ -145,6 +178,10 @@ def test_mixtral_decode_t32_full(mixtral_experts):
 
 def test_mixtral_prefill_t4096_sampled(mixtral_experts):
     _mixtral_case("prefill_t4096", mixtral_experts, 48)
+
+
+def test_mixtral_prefill_t4096_single_cta(mixtral_experts):
+    _mixtral_case("prefill_t4096", mixtral_experts, 48, pair=1)
 
 
 def test_mixtral_skewed_t32768_sampled(mixtral_experts):
