@@ -27,6 +27,7 @@
 // memory and return.
 #include <cudaTypedefs.h>
 
+#include "combine_epi.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -63,6 +64,7 @@ struct TcArgs {
     const int32_t* perm;
     const float* topk_w;
     int w_policy;         // L2 policy of weight loads: 0 evict_first, 1 evict_normal, 2 evict_last
+    CombineArgs comb;     // MODE 1: fused combine into y (comb.cnt null: Ys only)
     KStatus st;
 };
 
@@ -241,6 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row = offsets[e] + rloc;
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * ACC_COLS) +
                                    (static_cast<uint32_t>(q * 32) << 16);
+            int a = 0;
             if (MODE == 0) {
                 __nv_bfloat16* hrow = p.H + static_cast<size_t>(valid ? row : 0) * p.ldH + nb * 128;
 #pragma unroll 1
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             } else {
-                const int a = valid ? p.perm[row] : 0;
+                a = valid ? p.perm[row] : 0;
                 const float g = valid ? p.topk_w[a] : 0.0f;
                 float* yrow = p.Ys + static_cast<size_t>(a) * p.ldY + nb * 256;
 #pragma unroll 1
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_before();
             mbar_arrive(acce_bar(acc));
+            if (MODE == 1 && p.comb.cnt) combine_arrive(p.comb, p.Ys, p.ldY, valid, a, nb, lane);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -362,8 +366,8 @@ cudaError_t launch_tc_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1,
 }
 
 cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, const int* sched, int n, int d, int F,
-                            int R, float* Ys, const int32_t* perm, const float* topk_w, KStatus st, int num_sms,
-                            cudaStream_t s) {
+                            int R, float* Ys, const int32_t* perm, const float* topk_w, const CombineArgs& comb,
+                            KStatus st, int num_sms, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     if (n > MAX_EXPERTS) return cudaErrorInvalidValue;
     TcArgs args{};
@@ -376,6 +380,7 @@ cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, c
     args.ldY = d;
     args.perm = perm;
     args.topk_w = topk_w;
+    args.comb = comb;
     args.st = st;
     return launch_tc<1>(mapH, mapW2, mapW2, args, num_sms, s);
 }

@@ -35,6 +35,7 @@
 // memory is freed and before either CTA exits.
 #include <cudaTypedefs.h>
 
+#include "combine_epi.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -69,6 +70,7 @@ struct PairArgs {
     int ldY;
     const int32_t* perm;
     const float* topk_w;
+    CombineArgs comb;     // MODE 1: fused combine into y (comb.cnt null: Ys only)
     KStatus st;
 };
 
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             const int row = offsets[e] + rloc;
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * Q_ACC_COLS) +
                                    (static_cast<uint32_t>(q * 32) << 16);
+            int a = 0;
             if (MODE == 0) {
                 __nv_bfloat16* hrow = p.H + static_cast<size_t>(valid ? row : 0) * p.ldH + nb * 128;
 #pragma unroll 1
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
                     }
                 }
             } else {
-                const int a = valid ? p.perm[row] : 0;
+                a = valid ? p.perm[row] : 0;
                 const float g = valid ? p.topk_w[a] : 0.0f;
                 float* yrow = p.Ys + static_cast<size_t>(a) * p.ldY + nb * 256;
 #pragma unroll 1
@@ -300,6 +303,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8u * acc);
+            if (MODE == 1 && p.comb.cnt) combine_arrive(p.comb, p.Ys, p.ldY, valid, a, nb, lane);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -403,8 +407,8 @@ cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW
 }
 
 cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_128, const int* sched, int n, int d,
-                              int F, int R, float* Ys, const int32_t* perm, const float* topk_w, KStatus st,
-                              int num_sms, cudaStream_t s) {
+                              int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
+                              const CombineArgs& comb, KStatus st, int num_sms, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     if (n > Q_MAX_EXPERTS) return cudaErrorInvalidValue;
     PairArgs args{};
@@ -417,6 +421,7 @@ cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_
     args.ldY = d;
     args.perm = perm;
     args.topk_w = topk_w;
+    args.comb = comb;
     args.st = st;
     return launch_pair<1>(mapH, mapW2_128, mapW2_128, args, num_sms, s);
 }

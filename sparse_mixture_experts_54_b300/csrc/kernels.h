@@ -7,6 +7,7 @@
 
 #include <utility>
 
+#include "combine_epi.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -47,6 +48,16 @@ cudaError_t launch_gather(ElemType et, const void* x, const int32_t* perm, int R
                           void* Xp, cudaStream_t s);
 cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, void* y, cudaStream_t s);
 
+// Router + top-k + dispatch + row gather in one kernel (route_fused.cu).  xchg
+// holds fused_route_xchg_ints() ints that must be zero before the first call;
+// every complete call leaves them as it found them.  Xp and logits may be null.
+constexpr int kFusedRouteMaxBlocks = 160;
+inline int fused_route_xchg_ints() { return 2 + kFusedRouteMaxBlocks * 32; }
+int fused_route_blocks(int T, int num_sms);
+cudaError_t launch_fused_route(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d, int n,
+                               int K, int32_t* topk_idx, float* topk_w, float* logits, int* sched, int32_t* perm,
+                               int32_t* inv, void* Xp, int* xchg, KStatus st, int num_sms, cudaStream_t s);
+
 // CUDA-core grouped GEMMs (fp32 path) ------------------------------------------
 cudaError_t launch_simt_gemm13(ElemType et, const void* Xp, const void* W1, const void* W3, void* H,
                                const int* sched, int n, int d, int F, int R, cudaStream_t s);
@@ -60,9 +71,10 @@ bool encode_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint6
 cudaError_t launch_tc_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1,
                              const CUtensorMap& mapW3, const int* sched, int n, int d, int F, int R,
                              __nv_bfloat16* H, KStatus st, int num_sms, cudaStream_t s);
+// comb.cnt non-null: the epilogue also does the combine (combine_epi.cuh) and writes y.
 cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, const int* sched, int n,
                             int d, int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
-                            KStatus st, int num_sms, cudaStream_t s);
+                            const CombineArgs& comb, KStatus st, int num_sms, cudaStream_t s);
 
 // tcgen05 grouped GEMMs on CTA pairs (cta_group::2; 256-row tiles) -------------
 bool pair_gemm_available(int num_sms);
@@ -70,8 +82,8 @@ cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW
                                const int* sched, int n, int d, int F, int R, __nv_bfloat16* H, KStatus st,
                                int num_sms, cudaStream_t s);
 cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_128, const int* sched, int n, int d,
-                              int F, int R, float* Ys, const int32_t* perm, const float* topk_w, KStatus st,
-                              int num_sms, cudaStream_t s);
+                              int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
+                              const CombineArgs& comb, KStatus st, int num_sms, cudaStream_t s);
 
 // weight-streaming decode path (bf16, small T) ----------------------------------
 constexpr int kDecodeMaxT = 256;     // tokens per call the decode kernels accept

@@ -33,6 +33,8 @@ struct moe_ctx {
     int32_t* perm = nullptr;
     int32_t* inv = nullptr;
     int* sched = nullptr;
+    int* xchg = nullptr;        // grid-barrier words and block counts of the fused routing kernel
+    int* ccnt = nullptr;        // [T][d/256] arrival counters of the combine fused into the W2 epilogue
     void* Xp = nullptr;
     void* H = nullptr;
     float* Ys = nullptr;
@@ -46,7 +48,7 @@ struct moe_ctx {
     // per-stage CUDA-event timing (MOE_OPT_STAGE_TIMING)
     bool stage_timing = false;
     std::vector<cudaEvent_t> ev_free;
-    std::vector<std::array<cudaEvent_t, 8>> ev_calls;
+    std::vector<std::array<cudaEvent_t, 5>> ev_calls;
 };
 
 namespace {
@@ -55,7 +57,7 @@ size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t topk_idx, topk_w, perm, inv, sched, Xp, H, Ys, xbuf, ybuf, Pa, Pb, P2, total;
+    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, Xp, H, Ys, xbuf, ybuf, Pa, Pb, P2, total;
 };
 
 Layout layout_for(const moe_ctx* c, int T, int Tdec) {
@@ -70,6 +72,8 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.perm = take(R * 4);
     L.inv = take(R * 4);
     L.sched = take(static_cast<size_t>(sched_ints(c->n)) * 4);
+    L.xchg = take(static_cast<size_t>(fused_route_xchg_ints()) * 4);
+    L.ccnt = take(Tn * static_cast<size_t>((c->d + 255) / 256) * 4);
     L.Xp = take(R * c->d * es);
     L.H = take(R * c->F * es);
     L.Ys = take(R * c->d * 4);
@@ -135,6 +139,8 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->perm = reinterpret_cast<int32_t*>(b + L.perm);
     c->inv = reinterpret_cast<int32_t*>(b + L.inv);
     c->sched = reinterpret_cast<int*>(b + L.sched);
+    c->xchg = reinterpret_cast<int*>(b + L.xchg);
+    c->ccnt = reinterpret_cast<int*>(b + L.ccnt);
     c->Xp = b + L.Xp;
     c->H = b + L.H;
     c->Ys = reinterpret_cast<float*>(b + L.Ys);
@@ -145,6 +151,7 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->P2 = reinterpret_cast<float*>(b + L.P2);
     c->cap_T = T;
     c->cap_dec = Tdec;
+    if (cudaMemsetAsync(c->xchg, 0, L.Xp - L.xchg, s) != cudaSuccess) return MOE_ERR_CUDA;   // xchg + ccnt
     // Tensor maps of the workspace activations cover the full capacity; rows
     // beyond the live K*T are never valid rows of any tile.
     if (c->dtype == MOE_BF16) {
@@ -177,15 +184,14 @@ bool use_pair(const moe_ctx* c) {
 }
 
 // Stages of one forward call, in launch order.
-constexpr int kStages = 6;
-const char* const kStageNames[kStages] = {"router", "dispatch", "gather", "expert_w1w3_swiglu",
-                                          "expert_w2_gate", "combine"};
+constexpr int kStages = 4;
+const char* const kStageNames[kStages] = {"route", "expert_w1w3_swiglu", "expert_w2_gate", "combine"};
 
 // Events of the current call when stage timing is on (null otherwise).
 struct StageMarks {
     moe_ctx* c = nullptr;
     cudaStream_t s = nullptr;
-    std::array<cudaEvent_t, 8> ev{};
+    std::array<cudaEvent_t, 5> ev{};
     bool on = false;
     StageMarks(moe_ctx* ctx, cudaStream_t st) : c(ctx), s(st) {
         if (!c->stage_timing) return;
@@ -216,16 +222,13 @@ struct StageMarks {
     }
 };
 
-// router + top-k + dispatch into the workspace
-int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s, float* logits) {
+// router + top-k + dispatch (+ the row gather into Xp when gather is set)
+int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s, float* logits, bool gather) {
     const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
-    const int R = c->k * T;
-    cudaError_t e = launch_router(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, logits,
-                                  c->num_sms, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_dispatch(c->topk_idx, R, c->n, c->sched, c->perm, c->inv, kstatus(c), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return MOE_OK;
+    cudaError_t e = launch_fused_route(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, logits,
+                                       c->sched, c->perm, c->inv, gather ? c->Xp : nullptr, c->xchg, kstatus(c),
+                                       c->num_sms, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
 int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
@@ -233,23 +236,17 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
     const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
     const int R = c->k * T;
     StageMarks marks(c, s);
-    cudaError_t e = launch_router(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, nullptr,
-                                  c->num_sms, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    int rc = run_route(c, x, Wg, T, s, nullptr, true);
+    if (rc != MOE_OK) return rc;
     marks.mark(0);
-    e = launch_dispatch(c->topk_idx, R, c->n, c->sched, c->perm, c->inv, kstatus(c), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(1);
-    e = launch_gather(et, x, c->perm, R, c->k, c->d, c->Xp, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(2);
+    cudaError_t e = cudaSuccess;
     if (et == ElemType::F32) {
         e = launch_simt_gemm13(et, c->Xp, W1, W3, c->H, c->sched, c->n, c->d, c->F, R, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(3);
+        marks.mark(1);
         e = launch_simt_gemm2(et, c->H, W2, c->Ys, c->sched, c->perm, c->topk_w, c->n, c->d, c->F, R, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(4);
+        marks.mark(2);
     } else if (use_decode(c, T)) {
         CUtensorMap mW1, mW3, mW2;
         const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
@@ -265,13 +262,13 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         if (e != cudaSuccess) return cuda_fail(e);
         e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(3);
+        marks.mark(1);
         e = launch_decode_w2(mW2, c->map_H32, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(4);
+        marks.mark(2);
         e = launch_decode_combine(et, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, y, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(5);
+        marks.mark(3);
         marks.finish();
         return MOE_OK;
     } else {
@@ -290,19 +287,28 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
             e = launch_tc_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
                                  static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(3);
+        marks.mark(1);
+        CombineArgs comb{};
+        comb.cnt = c->ccnt;
+        comb.y = static_cast<__nv_bfloat16*>(y);
+        comb.K = c->k;
+        comb.nblk = c->d / 256;
+        comb.d = c->d;
         if (pair)
-            e = launch_pair_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, st,
+            e = launch_pair_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, comb, st,
                                   c->num_sms, s);
         else
-            e = launch_tc_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, st,
+            e = launch_tc_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, comb, st,
                                 c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(4);
+        marks.mark(2);
+        marks.mark(3);   // the combine ran inside the W2 epilogue
+        marks.finish();
+        return MOE_OK;
     }
     e = launch_combine(et, c->Ys, T, c->k, c->d, y, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(5);
+    marks.mark(3);
     marks.finish();
     return MOE_OK;
 }
@@ -415,7 +421,7 @@ int moe_route(moe_ctx* c, const void* x, const float* Wg, int T, int32_t* topk_i
     int rc = ensure_workspace(c, T, s);
     if (rc != MOE_OK) return rc;
     if (T > 0) {
-        rc = run_route(c, x, Wg, T, s, nullptr);
+        rc = run_route(c, x, Wg, T, s, nullptr, false);
         if (rc != MOE_OK) return rc;
     } else {
         if (cudaMemsetAsync(c->sched, 0, sched_ints(c->n) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -438,10 +444,7 @@ int moe_router_logits(moe_ctx* c, const void* x, const float* Wg, int T, float* 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int rc = ensure_workspace(c, T, s);
     if (rc != MOE_OK) return rc;
-    const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
-    cudaError_t e = launch_router(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, logits,
-                                  c->num_sms, s);
-    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+    return run_route(c, x, Wg, T, s, logits, false);
 }
 
 int moe_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
@@ -486,6 +489,17 @@ int moe_status(moe_ctx* c) {
 
 int moe_clear_status(moe_ctx* c) {
     if (!c) return MOE_ERR_INVALID;
+    // A call that gave up (a bounded wait ran out) can leave the routing
+    // kernel's barrier words or the fused combine's counters mid-count: put
+    // them back (synchronously, on the device of the context).
+    if (c->xchg && (*reinterpret_cast<volatile int*>(c->status_host) & kStatusTimeout)) {
+        if (cudaDeviceSynchronize() != cudaSuccess ||
+            cudaMemset(c->xchg, 0, static_cast<size_t>(reinterpret_cast<char*>(c->Xp) - reinterpret_cast<char*>(c->xchg))) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+    }
     *reinterpret_cast<volatile int*>(c->status_host) = 0;
     return MOE_OK;
 }

@@ -131,7 +131,8 @@ extern "C" int moe_forward_noalloc(const void* x, const float* W_g, const float*
             e = launch_tc_gemm13(mXp, mW1, mW3, sched, n_experts, d, d_ff, Ri, static_cast<__nv_bfloat16*>(H), st,
                                  sms, s);
             if (e == cudaSuccess)
-                e = launch_tc_gemm2(mH, mW2, sched, n_experts, d, d_ff, Ri, Ys, perm, topk_w, st, sms, s);
+                e = launch_tc_gemm2(mH, mW2, sched, n_experts, d, d_ff, Ri, Ys, perm, topk_w, CombineArgs{}, st,
+                                    sms, s);
         }
     }
     if (e == cudaSuccess) e = launch_combine(et, Ys, T, k, d, y, s);

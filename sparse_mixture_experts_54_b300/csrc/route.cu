@@ -7,73 +7,9 @@
 // Dispatch replaces the one_hot/permute/where walk and the row gather of
 // aiqianji 3.1.2 (code blocks B, C); combine replaces index_add_ there.
 #include "kernels.h"
+#include "route_common.cuh"
 
 namespace moe {
-
-// ---------------------------------------------------------------------------
-// 8 consecutive elements of a row as fp32 (zeros past the end of the row).
-template <typename TX>
-__device__ __forceinline__ void load8(const TX* row, int j0, int d, float (&v)[8]) {
-    if (j0 >= d) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = 0.0f;
-        return;
-    }
-    if constexpr (sizeof(TX) == 2) {
-        uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + j0));
-        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __bfloat162float(h[u]);
-    } else {
-        float4 a = __ldg(reinterpret_cast<const float4*>(row + j0));
-        float4 b = __ldg(reinterpret_cast<const float4*>(row + j0 + 4));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-}
-
-// acc + sum_u x[u] * w[u] over 8 elements, fused multiply-adds in index order.
-__device__ __forceinline__ float dot8(const float (&xv)[8], const float* w, float acc) {
-    float4 w0 = *reinterpret_cast<const float4*>(w);
-    float4 w1 = *reinterpret_cast<const float4*>(w + 4);
-    acc = fmaf(xv[0], w0.x, acc); acc = fmaf(xv[1], w0.y, acc);
-    acc = fmaf(xv[2], w0.z, acc); acc = fmaf(xv[3], w0.w, acc);
-    acc = fmaf(xv[4], w1.x, acc); acc = fmaf(xv[5], w1.y, acc);
-    acc = fmaf(xv[6], w1.z, acc); acc = fmaf(xv[7], w1.w, acc);
-    return acc;
-}
-
-// Top-k and gate from the n logits held (identically) by every lane of a warp:
-// lane e ranks its own expert (number of experts with a larger logit, or an
-// equal logit at a lower index); the K best write their slot.  Softmax over
-// the kept logits only (the others are -inf), shifted by the maximum.
-template <int NMAX>
-__device__ __forceinline__ void topk_gate_write(const float (&l)[NMAX], int n, int K, int t, int lane,
-                                                int32_t* topk_idx, float* topk_w, float* logits_out) {
-    float mine = 0.0f, lmax = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e) {
-        if (e < n) {
-            if (e == lane) mine = l[e];
-            lmax = fmaxf(lmax, l[e]);
-        }
-    }
-    int rank = 0;
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e) {
-        if (e < n) rank += (l[e] > mine) || (l[e] == mine && e < lane);
-    }
-    const bool kept = lane < n && rank < K;
-    const float num = kept ? expf(mine - lmax) : 0.0f;
-    float z = num;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (kept) {
-        topk_idx[static_cast<size_t>(t) * K + rank] = lane;
-        topk_w[static_cast<size_t>(t) * K + rank] = num / z;
-    }
-    if (logits_out && lane < n) logits_out[static_cast<size_t>(t) * n + lane] = mine;
-}
 
 // ---------------------------------------------------------------------------
 // Router for small batches: one block of 8 warps per token.  Warp w sums the

@@ -1,0 +1,458 @@
+// route_fused.cu -- router, dispatch and row gather of the MoE layer in one
+// kernel.
+//
+// What it computes is exactly what the separate router, dispatch and gather
+// kernels of route.cu compute (the pages' gate and the one_hot/where walk with
+// its hidden_states[top_x] gather, aiqianji 2.1.1 and 3.1.2, code blocks B/C),
+// organised so that no step runs on a single block:
+//
+//   phase 1  every block routes one contiguous range of tokens: fp32 logits
+//            x . W_g^T (+ bias) with W_g staged in shared memory, top-k and the
+//            softmax over the kept logits, plus the block's per-expert counts;
+//   barrier  the blocks publish their counts and meet at one grid-wide
+//            barrier (all blocks are resident: one per SM at most);
+//   phase 2  every block reads all blocks' counts, so it knows the expert
+//            offsets and how many rows of each expert the blocks before it own;
+//            it places its own assignments a = t*K + slot at
+//            offsets[e] + (rows of e in earlier blocks) + (rank among its own
+//            rows of e, in a order) -- the stable expert-contiguous order -- and
+//            copies their token rows into Xp.
+//
+// Block b's tokens precede block b+1's, so the order is the same as a single
+// pass over all assignments would give.  Nothing depends on timing: counts are
+// order-free sums and every position follows from them.
+//
+// Logits: block of 16 warps = 4 token groups x 4 warps that split the row;
+// warp (g, q) takes the 256-element segments q, q+4, q+8, ... of the row, and
+// in each segment lane l takes elements [4l, 4l+4) and [128+4l, 128+4l+4), so
+// a warp's float4 reads of W_g cover 512 contiguous bytes (no shared-memory
+// bank conflicts) and its x reads are coalesced.  A lane accumulates in
+// segment order, the 32 lanes are added by a fixed transpose-and-add pattern,
+// and the 4 quarter sums are added in q order before the bias.  The same
+// arithmetic serves moe_route, moe_router_logits and moe_forward.
+//
+// The grid barrier: a count and a generation word in the context workspace.
+// Each block reads the generation, adds 1 to the count; the last arrival
+// resets the count to 0 and advances the generation, the others wait for it
+// to advance (bounded; on expiry the block records a timeout and leaves).  The
+// words return to their starting state after every complete call, so a CUDA
+// graph can replay the launch.  Dependent kernels are released only after
+// every block has passed the barrier, so the next call's blocks can never
+// meet this call's.
+#include "kernels.h"
+#include "route_common.cuh"
+
+namespace moe {
+
+namespace {
+constexpr int FR_THREADS = 512;
+constexpr int FR_WARPS = 16;
+constexpr int FR_DS = 4;                    // warps that split one row
+constexpr int FR_TG = FR_WARPS / FR_DS;     // token groups per block
+constexpr int FR_ROUND = FR_THREADS;        // assignments placed per round in phase 2
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+}  // namespace
+
+struct FusedRouteArgs {
+    const void* x;
+    const float* Wg;
+    const float* bias;
+    int T, d, n, K;
+    int chunk;              // tokens per block (the last block may have fewer)
+    int32_t* topk_idx;      // [T*K]
+    float* topk_w;          // [T*K]
+    float* logits;          // optional [T][n]
+    int* sched;             // counts, offsets, 128-row tile prefix
+    int32_t* perm;          // [T*K]
+    int32_t* inv;           // [T*K]
+    void* Xp;               // optional [T*K][d]: gathered rows
+    int row_vecs;           // 16-byte vectors per row of x
+    int* xchg;              // [0] count, [1] generation, [2 + 32*b + e] block counts
+    size_t red_off;         // byte offset of the lane-sum buffer in dynamic shared memory
+    KStatus st;
+};
+
+// Sum over the 32 lanes of V values per lane (V a power of two).  Each step
+// trades half of the values with the partner lane and adds, halving the count,
+// until one value per lane is left; remaining steps are plain butterflies.
+// Afterwards lane l holds the full sums of value indices fr_index(l, i),
+// i < max(V/32, 1).
+template <int V>
+__device__ __forceinline__ void lane_transpose_sum(float (&v)[V], int lane) {
+    int cur = V;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        if (cur > 1) {
+            const int half = cur >> 1;
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < half) {
+                    const float send = up ? v[i] : v[half + i];
+                    const float keep = up ? v[half + i] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            cur = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+}
+// 4 consecutive elements of a row as fp32 (zeros when !ok).
+template <typename TX>
+__device__ __forceinline__ void load4(const TX* row, int j0, bool ok, float* v) {
+    if (!ok) {
+        v[0] = v[1] = v[2] = v[3] = 0.0f;
+        return;
+    }
+    if constexpr (sizeof(TX) == 2) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row + j0));
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        v[0] = __low2float(lo);
+        v[1] = __high2float(lo);
+        v[2] = __low2float(hi);
+        v[3] = __high2float(hi);
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(row + j0));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    }
+}
+
+template <int V>
+__device__ __forceinline__ int fr_index(int lane, int i) {
+    int idx = i, cur = V;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        if (cur > 1) {
+            cur >>= 1;
+            if (lane & o) idx += cur;
+        }
+    }
+    return idx;
+}
+
+template <typename TX, int NMAX, int TOKW>
+__global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteArgs p) {
+    extern __shared__ __align__(16) unsigned char fr_smem[];
+    float* wg_s = reinterpret_cast<float*>(fr_smem);
+    float* red = reinterpret_cast<float*>(fr_smem + p.red_off);   // [FR_DS][TPB][NMAX]
+    __shared__ int s_hist[32], s_cnt[32], s_pre[32], s_base[32], s_run[32];
+    __shared__ int wtab[FR_WARPS][33];
+    __shared__ int s_ok;
+    constexpr int TPB = FR_TG * TOKW;   // tokens per block iteration
+    constexpr int V = TOKW * NMAX;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = p.n, d = p.d, K = p.K;
+    const int b = blockIdx.x, G = gridDim.x;
+
+    // W_g is written by no kernel of the layer: stage it before waiting on the
+    // previous kernel.
+    {
+        const int total4 = n * d / 4;
+        const float4* src = reinterpret_cast<const float4*>(p.Wg);
+        float4* dst = reinterpret_cast<float4*>(wg_s);
+        for (int i0 = tid; i0 < total4; i0 += 8 * FR_THREADS) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * FR_THREADS;
+                v[u] = i < total4 ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * FR_THREADS;
+                if (i < total4) dst[i] = v[u];
+            }
+        }
+    }
+    if (tid < 32) s_hist[tid] = 0;
+    griddep_wait();
+    __syncthreads();
+
+    // ---------------- phase 1: logits, top-k, gates, block counts ----------------
+    const int t_begin = b * p.chunk;
+    const int t_end = min(p.T, t_begin + p.chunk);
+    const TX* x = static_cast<const TX*>(p.x);
+    const int tg = warp / FR_DS, q = warp % FR_DS;
+    for (int tb = t_begin; tb < t_end; tb += TPB) {
+        float acc[TOKW][NMAX];
+#pragma unroll
+        for (int j = 0; j < TOKW; ++j)
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e) acc[j][e] = 0.0f;
+        const int t0 = tb + tg * TOKW;
+        for (int sg = q; sg * 256 < d; sg += FR_DS) {
+            const int j0 = sg * 256 + 4 * lane, j1 = j0 + 128;
+            const bool h0 = j0 < d, h1 = j1 < d;
+            float xv[TOKW][8];
+#pragma unroll
+            for (int j = 0; j < TOKW; ++j) {
+                const TX* row = x + static_cast<size_t>(t0 + j) * d;
+                const bool tv = t0 + j < t_end;
+                load4(row, j0, tv && h0, &xv[j][0]);
+                load4(row, j1, tv && h1, &xv[j][4]);
+            }
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e) {
+                if (e < n) {
+                    const float* w = wg_s + static_cast<size_t>(e) * d;
+                    const float4 w0 = h0 ? *reinterpret_cast<const float4*>(w + j0) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 w1 = h1 ? *reinterpret_cast<const float4*>(w + j1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int j = 0; j < TOKW; ++j) {
+                        float a = acc[j][e];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) a = fmaf(xv[j][u], wv[u], a);
+                        acc[j][e] = a;
+                    }
+                }
+            }
+        }
+        float v[V];
+#pragma unroll
+        for (int j = 0; j < TOKW; ++j)
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e) v[j * NMAX + e] = acc[j][e];
+        lane_transpose_sum<V>(v, lane);
+        constexpr int VF = V >= 32 ? V / 32 : 1;
+#pragma unroll
+        for (int i = 0; i < VF; ++i) {
+            const int idx = fr_index<V>(lane, i);   // = j * NMAX + e of this warp's tokens
+            red[(q * TPB + tg * TOKW) * NMAX + idx] = v[i];
+        }
+        __syncthreads();
+        for (int j = warp; j < TPB; j += FR_WARPS) {
+            const int t = tb + j;
+            if (t < t_end) {
+                float l[NMAX];
+#pragma unroll
+                for (int e = 0; e < NMAX; ++e) {
+                    float s = 0.0f;
+                    if (e < n) {
+#pragma unroll
+                        for (int qq = 0; qq < FR_DS; ++qq) s += red[(qq * TPB + j) * NMAX + e];
+                        if (p.bias) s += __ldg(p.bias + e);
+                    }
+                    l[e] = s;
+                }
+                topk_gate_write<NMAX>(l, n, K, t, lane, p.topk_idx, p.topk_w, p.logits, s_hist);
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---------------- grid barrier: publish and collect the block counts ----------------
+    int* cnt_word = p.xchg;
+    int* gen_word = p.xchg + 1;
+    int* bcounts = p.xchg + 2;
+    if (tid < 32) bcounts[b * 32 + tid] = tid < n ? s_hist[tid] : 0;
+    __syncthreads();
+    if (tid == 0) {
+        const int g = ld_acquire_gpu(gen_word);
+        __threadfence();
+        const int prev = atomicAdd(cnt_word, 1);
+        int ok = 1;
+        if (prev == G - 1) {
+            atomicExch(cnt_word, 0);
+            __threadfence();
+            st_release_gpu(gen_word, g + 1);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            uint32_t it = 0;
+            while (ld_acquire_gpu(gen_word) == g) {
+                if ((++it & 63u) == 0 && globaltimer_ns() - t0 > p.st.wait_ns) {
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) {
+        if (tid == 0) report(p.st, kStatusTimeout);
+        return;
+    }
+    // Every block has passed the barrier: later kernels may start their prologues.
+    griddep_launch_dependents();
+
+    // ---------------- phase 2: offsets, stable positions, row gather ----------------
+    // Totals and this block's prefix per expert: warp w sums expert w (and
+    // w + 16) over the blocks, lane-strided, then across lanes (integer sums:
+    // the order does not matter).
+    for (int e = warp; e < n; e += FR_WARPS) {
+        int tot = 0, pre = 0;
+        for (int bb = lane; bb < G; bb += 32) {
+            const int c = __ldcg(bcounts + bb * 32 + e);
+            tot += c;
+            pre += bb < b ? c : 0;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            tot += __shfl_xor_sync(0xffffffffu, tot, off);
+            pre += __shfl_xor_sync(0xffffffffu, pre, off);
+        }
+        if (lane == 0) {
+            s_cnt[e] = tot;
+            s_pre[e] = pre;
+        }
+    }
+    if (tid < 32) s_run[tid] = 0;
+    __syncthreads();
+    if (tid == 0) {
+        int running = 0, tp = 0;
+        for (int e = 0; e < n; ++e) {
+            const int c = s_cnt[e];
+            s_base[e] = running + s_pre[e];
+            if (b == 0) {
+                p.sched[e] = c;
+                p.sched[n + e] = running;
+                p.sched[2 * n + 1 + e] = tp;
+            }
+            running += c;
+            tp += (c + kTileM - 1) / kTileM;
+        }
+        if (b == 0) {
+            p.sched[2 * n] = running;
+            p.sched[3 * n + 1] = tp;
+        }
+    }
+    __syncthreads();
+
+    int2* placed = reinterpret_cast<int2*>(fr_smem);   // [FR_ROUND]; W_g is no longer read
+    const int a_begin = t_begin * K, a_end = t_end * K;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const uint4* xv4 = static_cast<const uint4*>(p.x);
+    uint4* xp4 = static_cast<uint4*>(p.Xp);
+    for (int a0 = a_begin; a0 < a_end; a0 += FR_ROUND) {
+        const int a = a0 + tid;
+        const int e = a < a_end ? p.topk_idx[a] : -1;   // this block's own phase-1 writes
+        wtab[warp][lane] = 0;
+        __syncwarp();
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & lt_mask);
+        if (e >= 0 && rank == 0) wtab[warp][e] = __popc(same);
+        __syncthreads();
+        // per expert: exclusive scan of the 16 warps' counts, in warp order
+        for (int ee = warp; ee < n; ee += FR_WARPS) {
+            const int cnt = lane < FR_WARPS ? wtab[lane][ee] : 0;
+            const int run = s_run[ee];
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (lane < FR_WARPS) wtab[lane][ee] = run + incl - cnt;
+            __syncwarp();
+            if (lane == 31) s_run[ee] = run + incl;
+        }
+        __syncthreads();
+        if (e >= 0) {
+            const int pos = s_base[e] + wtab[warp][e] + rank;
+            p.perm[pos] = a;
+            p.inv[a] = pos;
+            placed[tid] = make_int2(a, pos);
+        }
+        __syncthreads();
+        if (xp4) {
+            const int nr = min(FR_ROUND, a_end - a0);
+            const int rv = p.row_vecs;
+            for (int r = warp; r < nr; r += FR_WARPS) {
+                const int2 ap = placed[r];
+                const uint4* src = xv4 + static_cast<size_t>(ap.x / K) * rv;
+                uint4* dst = xp4 + static_cast<size_t>(ap.y) * rv;
+                for (int v0 = lane; v0 < rv; v0 += 32 * 8) {
+                    uint4 buf[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int vv = v0 + 32 * u;
+                        if (vv < rv) buf[u] = __ldg(src + vv);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int vv = v0 + 32 * u;
+                        if (vv < rv) dst[vv] = buf[u];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+int fused_route_blocks(int T, int num_sms) {
+    if (T <= 0) return 0;
+    int g = num_sms < kFusedRouteMaxBlocks ? num_sms : kFusedRouteMaxBlocks;
+    if (g > T) g = T;
+    const int chunk = (T + g - 1) / g;
+    return (T + chunk - 1) / chunk;
+}
+
+template <typename TX, int NMAX, int TOKW>
+static cudaError_t launch_fused_t(FusedRouteArgs& a, int G, cudaStream_t s) {
+    constexpr int TPB = FR_TG * TOKW;
+    const size_t wg_bytes = static_cast<size_t>(a.n) * a.d * 4;
+    const size_t p2_bytes = FR_ROUND * sizeof(int2);
+    size_t base = wg_bytes > p2_bytes ? wg_bytes : p2_bytes;
+    base = (base + 15) & ~static_cast<size_t>(15);
+    a.red_off = base;
+    const size_t smem = base + static_cast<size_t>(FR_DS) * TPB * NMAX * 4;
+    auto kern = route_fused_kernel<TX, NMAX, TOKW>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(G), dim3(FR_THREADS), smem, s, a);
+}
+
+cudaError_t launch_fused_route(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d, int n,
+                               int K, int32_t* topk_idx, float* topk_w, float* logits, int* sched, int32_t* perm,
+                               int32_t* inv, void* Xp, int* xchg, KStatus st, int num_sms, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    if (n > 32) return cudaErrorInvalidValue;
+    const int G = fused_route_blocks(T, num_sms);
+    FusedRouteArgs a{};
+    a.x = x;
+    a.Wg = Wg;
+    a.bias = bias;
+    a.T = T;
+    a.d = d;
+    a.n = n;
+    a.K = K;
+    a.chunk = (T + G - 1) / G;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.logits = logits;
+    a.sched = sched;
+    a.perm = perm;
+    a.inv = inv;
+    a.Xp = Xp;
+    a.row_vecs = d * (et == ElemType::BF16 ? 2 : 4) / 16;
+    a.xchg = xchg;
+    a.st = st;
+    if (et == ElemType::BF16) {
+        if (n <= 8) return launch_fused_t<__nv_bfloat16, 8, 4>(a, G, s);
+        if (n <= 16) return launch_fused_t<__nv_bfloat16, 16, 2>(a, G, s);
+        return launch_fused_t<__nv_bfloat16, 32, 1>(a, G, s);
+    }
+    if (n <= 8) return launch_fused_t<float, 8, 4>(a, G, s);
+    if (n <= 16) return launch_fused_t<float, 16, 2>(a, G, s);
+    return launch_fused_t<float, 32, 1>(a, G, s);
+}
+
+}  // namespace moe
