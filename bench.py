@@ -37,6 +37,34 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s (T=4096 prefill) & µs/layer decode T=32; % of BF16/HBM roofline"
 
 
+# DRAM traffic of the dominant kernel (W1/W3 grouped GEMM) per launch at the
+# prefill workload, from one ncu capture, kept with a hash of the sources that
+# define the kernel: the figure is reported only while they are unchanged.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_w13_prefill_t4096.json")
+W13_SOURCES = [os.path.join(ROOT, "sparse_mixture_experts_54_b300", "csrc", f)
+               for f in ("gemm_tc.cu", "common.cuh", "combine_epi.cuh")]
+
+
+def w13_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in W13_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def w13_traffic():
+    """(bytes per launch, note) from the committed capture, or (None, why)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no capture committed"
+    with open(TRAFFIC_FILE) as f:
+        t = json.load(f)
+    if t.get("source_sha256") != w13_source_hash():
+        return None, "kernel changed since the capture"
+    return int(t["dram_bytes_per_launch"]), t.get("command", "")
+
+
 def peaks():
     p = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -243,12 +271,15 @@ def run_ours(args, rank, world, dist):
     # dominant kernel: the W1/W3 grouped GEMM (2/3 of the FLOPs)
     k13_ms = stages_p.get("expert_w1w3_swiglu", float("nan"))
     achieved = alg_p["flops_w13"] / (k13_ms * 1e-3) / 1e12
+    traffic, traffic_note = w13_traffic()
     roofline = {"kernel": "expert_w1w3_swiglu (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
                 "peak_kind": f"bf16 sustained ({pk['source']})",
                 "frac_of_burst": round(achieved / pk["bf16_tflops"], 4),
-                "traffic": None}
+                "flops_per_launch": alg_p["flops_w13"],
+                "traffic": traffic, "traffic_unit": "bytes per launch (dram read + write)",
+                "traffic_source": traffic_note}
     layer_tflops = alg_p["flops"] / (ms_p * 1e-3) / 1e12
     dec_gbs = alg_d["bytes"] / (ms_d * 1e-3) / 1e9
     line = {
@@ -276,7 +307,7 @@ def run_ours(args, rank, world, dist):
                 "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                 "d2h_bytes_per_step": int(yh.numel() * yh.element_size()),
                 "ms_per_step": round(ms_e2e, 4), "entry_point": "moe_forward_host"},
-        "gpu_launches": 6 * args.steps,   # kernels per prefill call x timed prefill calls
+        "gpu_launches": 3 * args.steps,   # route, W1/W3 GEMM, W2 GEMM (combine in its epilogue) per call
         "timing": {"prefill_steps": args.steps, "decode_steps": args.decode_steps,
                    "per_kernel": "CUDA events recorded by the library around each kernel on the call's stream"},
         "clocks": clocks,

@@ -286,7 +286,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_before();
             mbar_arrive(acce_bar(acc));
-            if (MODE == 1 && p.comb.cnt) combine_arrive(p.comb, p.Ys, p.ldY, valid, a, nb, lane);
+            if (MODE == 1 && p.comb.cnt) {
+                combine_arrive(p.comb, p.Ys, p.ldY, valid, a, 2 * nb, lane);
+                combine_arrive(p.comb, p.Ys, p.ldY, valid, a, 2 * nb + 1, lane);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }

@@ -21,8 +21,15 @@
 //   MODE 1: CTA r loads W2 rows nb*256 + 128r + [0, 128): columns are the
 //           tile's 256 output features in order.
 //
-// Expert groups are covered by 256-row tiles (the last one ragged: rows past
-// the group's end are computed and dropped in the epilogue).
+// Expert groups are covered by 256-row tiles, except that a group whose last
+// tile would hold at most 128 rows ends with a 128-row tile: an M = 128 pair
+// MMA, 64 rows from each CTA.  That shape fills all 128 lanes of each CTA's
+// tensor memory but only 128 columns: lanes 0-63 hold the 64 rows for output
+// columns 0-127 (the even CTA's half of B) and lanes 64-127 hold the same rows
+// for columns 128-255 (the odd CTA's half).  So in MODE 0 such a tile loads,
+// in CTA r, the W1 rows and then the W3 rows of features [64r, 64r+64) of the
+// tile's 128, and every lane again holds both halves of its SwiGLU products.
+// Rows past a group's end are computed and dropped in the epilogue.
 //
 // Roles (6 warps per CTA, both CTAs): warp 0 lane 0 issues the CTA's TMA loads;
 // their completion is counted on the even CTA's full barrier (which expects
@@ -74,9 +81,10 @@ struct PairArgs {
     KStatus st;
 };
 
-// tile -> (expert, 256-row block, N block); expert-major, then N block, then row block.
-__device__ __forceinline__ void pair_decode_tile(const int* prefix, int n, int ntiles, int tile, int& e, int& mb,
-                                                 int& nb) {
+// tile -> (expert, 256-row block, N block, 128-row tile?); expert-major, then N
+// block, then row block.
+__device__ __forceinline__ void pair_decode_tile(const int* prefix, const int* counts, int n, int ntiles, int tile,
+                                                 int& e, int& mb, int& nb, bool& half) {
     int k = 0;
     while (k + 1 < n && prefix[k + 1] * ntiles <= tile) ++k;
     const int mt = prefix[k + 1] - prefix[k];
@@ -84,12 +92,15 @@ __device__ __forceinline__ void pair_decode_tile(const int* prefix, int n, int n
     e = k;
     nb = local / mt;
     mb = local % mt;
+    const int rem = counts[k] - mb * Q_PAIR_ROWS;   // rows of the group from this tile on
+    half = rem <= 128;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(Q_THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, PairArgs p) {
+                        const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0h,
+                        const __grid_constant__ CUtensorMap tmB1h, PairArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t tiles_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -127,7 +138,11 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB0);
-        if (MODE == 0) tma_prefetch_desc(&tmB1);
+        if (MODE == 0) {
+            tma_prefetch_desc(&tmB1);
+            tma_prefetch_desc(&tmB0h);
+            tma_prefetch_desc(&tmB1h);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), Q_TMEM_COLS);
@@ -173,9 +188,13 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             bool ok = true;
             for (int tile = cid; tile < total && ok; tile += ncl) {
                 int e, mb, nb;
-                pair_decode_tile(prefix, n, p.ntiles, tile, e, mb, nb);
-                const int arow = offsets[e] + mb * Q_PAIR_ROWS + static_cast<int>(rank) * 128;
-                const int brow = e * p.b_rows_per_e + (MODE == 0 ? nb * 128 : nb * 256 + static_cast<int>(rank) * 128);
+                bool half;
+                pair_decode_tile(prefix, counts, n, p.ntiles, tile, e, mb, nb, half);
+                // A: this CTA's 128 rows (a 128-row tile uses the first 64 of them)
+                const int arow = offsets[e] + mb * Q_PAIR_ROWS + static_cast<int>(rank) * (half ? 64 : 128);
+                const int brow = e * p.b_rows_per_e +
+                                 (MODE == 0 ? nb * 128 + (half ? 64 * static_cast<int>(rank) : 0)
+                                            : nb * 256 + static_cast<int>(rank) * 128);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
                     const uint32_t a_dst = tiles_u32 + stage * Q_STAGE_BYTES;
@@ -183,7 +202,13 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
                     const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Q_STAGE_BYTES);
                     tma_load_2d_pair(a_dst, &tmA, full_leader, kb * Q_BK, arow, pol_act);
-                    tma_load_2d_pair(b_dst, mapB, full_leader, kb * Q_BK, brow, pol_w);
+                    if (MODE == 0 && half) {
+                        // 64 W1 rows then the 64 W3 rows of the same features
+                        tma_load_2d_pair(b_dst, &tmB0h, full_leader, kb * Q_BK, brow, pol_w);
+                        tma_load_2d_pair(b_dst + Q_B_BYTES / 2, &tmB1h, full_leader, kb * Q_BK, brow, pol_w);
+                    } else {
+                        tma_load_2d_pair(b_dst, mapB, full_leader, kb * Q_BK, brow, pol_w);
+                    }
                     ++issued;
                     if (++stage == Q_STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -206,13 +231,18 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     } else if (warp == 1) {
         if (rank == 0 && lane == 0) {
             // ---------------- MMA issuer (even CTA only) ----------------
-            constexpr uint32_t idesc = idesc_bf16_f32(2 * 128, Q_ACC_COLS);
+            constexpr uint32_t idesc_full = idesc_bf16_f32(2 * 128, Q_ACC_COLS);
+            constexpr uint32_t idesc_half = idesc_bf16_f32(2 * 64, Q_ACC_COLS);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = cid; tile < total && ok; tile += ncl) {
+                int e, mb, nb;
+                bool half;
+                pair_decode_tile(prefix, counts, n, p.ntiles, tile, e, mb, nb, half);
+                const uint32_t idesc = half ? idesc_half : idesc_full;
                 if (!mbar_wait_cluster(acce_bar(acc), acc_phase ^ 1u, st, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Q_ACC_COLS);
@@ -251,22 +281,33 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
         bool ok = true;
         for (int tile = cid; tile < total; tile += ncl) {
             int e, mb, nb;
-            pair_decode_tile(prefix, n, p.ntiles, tile, e, mb, nb);
+            bool half;
+            pair_decode_tile(prefix, counts, n, p.ntiles, tile, e, mb, nb, half);
             if (!mbar_wait_cluster(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const int rloc = mb * Q_PAIR_ROWS + static_cast<int>(rank) * 128 + q * 32 + lane;   // row in the expert
+            // Full tile: lane L of this CTA's tensor memory is tile row 128*rank + L,
+            // all 256 columns.  128-row tile: lane L is tile row 64*rank + (L % 64),
+            // and holds output columns [128*(L / 64), +128) in tensor-memory
+            // columns 0..127.
+            const int hcol = half ? (q >> 1) : 0;
+            const int rloc = mb * Q_PAIR_ROWS +
+                             (half ? static_cast<int>(rank) * 64 + (q & 1) * 32 + lane
+                                   : static_cast<int>(rank) * 128 + q * 32 + lane);   // row in the expert
             const bool valid = rloc < counts[e];
             const int row = offsets[e] + rloc;
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * Q_ACC_COLS) +
                                    (static_cast<uint32_t>(q * 32) << 16);
             int a = 0;
             if (MODE == 0) {
-                __nv_bfloat16* hrow = p.H + static_cast<size_t>(valid ? row : 0) * p.ldH + nb * 128;
+                // features of this thread: full tile nb*128 + [0,128) with W3 at column
+                // offset 128; 128-row tile nb*128 + 64*hcol + [0,64) with W3 at offset 64
+                const int nfeat = half ? 64 : 128;
+                __nv_bfloat16* hrow = p.H + static_cast<size_t>(valid ? row : 0) * p.ldH + nb * 128 + 64 * hcol;
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
+                for (int c = 0; c < nfeat; c += 32) {
                     uint32_t av[32], bv[32];
                     tmem_ld_32x32b_x32(tbase + c, av);
-                    tmem_ld_32x32b_x32(tbase + 128 + c, bv);
+                    tmem_ld_32x32b_x32(tbase + nfeat + c, bv);
                     tmem_ld_wait();
                     uint32_t packed[16];
 #pragma unroll
@@ -285,9 +326,10 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             } else {
                 a = valid ? p.perm[row] : 0;
                 const float g = valid ? p.topk_w[a] : 0.0f;
-                float* yrow = p.Ys + static_cast<size_t>(a) * p.ldY + nb * 256;
+                const int nout = half ? 128 : 256;
+                float* yrow = p.Ys + static_cast<size_t>(a) * p.ldY + nb * 256 + 128 * hcol;
 #pragma unroll 1
-                for (int c = 0; c < 256; c += 32) {
+                for (int c = 0; c < nout; c += 32) {
                     uint32_t ov[32];
                     tmem_ld_32x32b_x32(tbase + c, ov);
                     tmem_ld_wait();
@@ -303,7 +345,14 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8u * acc);
-            if (MODE == 1 && p.comb.cnt) combine_arrive(p.comb, p.Ys, p.ldY, valid, a, nb, lane);
+            if (MODE == 1 && p.comb.cnt) {
+                if (half) {
+                    combine_arrive(p.comb, p.Ys, p.ldY, valid, a, 2 * nb + hcol, lane);
+                } else {
+                    combine_arrive(p.comb, p.Ys, p.ldY, valid, a, 2 * nb, lane);
+                    combine_arrive(p.comb, p.Ys, p.ldY, valid, a, 2 * nb + 1, lane);
+                }
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -364,8 +413,8 @@ int pair_clusters(int num_sms) {
 }
 
 template <int MODE>
-cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, PairArgs args,
-                        int num_sms, cudaStream_t s) {
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0h,
+                        const CUtensorMap& b1h, PairArgs args, int num_sms, cudaStream_t s) {
     const int nc = pair_clusters<MODE>(num_sms);
     if (nc <= 0) return cudaErrorNotSupported;
     auto kern = tc_pair_gemm_kernel<MODE>;
@@ -383,15 +432,15 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, args);
+    return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, b0h, b1h, args);
 }
 }  // namespace
 
 bool pair_gemm_available(int num_sms) { return pair_clusters<0>(num_sms) > 0 && pair_clusters<1>(num_sms) > 0; }
 
 cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1, const CUtensorMap& mapW3,
-                               const int* sched, int n, int d, int F, int R, __nv_bfloat16* H, KStatus st,
-                               int num_sms, cudaStream_t s) {
+                               const CUtensorMap& mapW1_64, const CUtensorMap& mapW3_64, const int* sched, int n,
+                               int d, int F, int R, __nv_bfloat16* H, KStatus st, int num_sms, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     if (n > Q_MAX_EXPERTS) return cudaErrorInvalidValue;
     PairArgs args{};
@@ -403,7 +452,7 @@ cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW
     args.H = H;
     args.ldH = F;
     args.st = st;
-    return launch_pair<0>(mapXp, mapW1, mapW3, args, num_sms, s);
+    return launch_pair<0>(mapXp, mapW1, mapW3, mapW1_64, mapW3_64, args, num_sms, s);
 }
 
 cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_128, const int* sched, int n, int d,
@@ -423,7 +472,7 @@ cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_
     args.topk_w = topk_w;
     args.comb = comb;
     args.st = st;
-    return launch_pair<1>(mapH, mapW2_128, mapW2_128, args, num_sms, s);
+    return launch_pair<1>(mapH, mapW2_128, mapW2_128, mapW2_128, mapW2_128, args, num_sms, s);
 }
 
 }  // namespace moe

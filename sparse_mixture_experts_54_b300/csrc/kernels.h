@@ -78,9 +78,10 @@ cudaError_t launch_tc_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2, c
 
 // tcgen05 grouped GEMMs on CTA pairs (cta_group::2; 256-row tiles) -------------
 bool pair_gemm_available(int num_sms);
+// mapW1/mapW3: 128-row boxes; mapW1_64/mapW3_64: the same tensors with 64-row boxes.
 cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW1, const CUtensorMap& mapW3,
-                               const int* sched, int n, int d, int F, int R, __nv_bfloat16* H, KStatus st,
-                               int num_sms, cudaStream_t s);
+                               const CUtensorMap& mapW1_64, const CUtensorMap& mapW3_64, const int* sched, int n,
+                               int d, int F, int R, __nv_bfloat16* H, KStatus st, int num_sms, cudaStream_t s);
 cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_128, const int* sched, int n, int d,
                               int F, int R, float* Ys, const int32_t* perm, const float* topk_w,
                               const CombineArgs& comb, KStatus st, int num_sms, cudaStream_t s);

@@ -34,7 +34,7 @@ struct moe_ctx {
     int32_t* inv = nullptr;
     int* sched = nullptr;
     int* xchg = nullptr;        // grid-barrier words and block counts of the fused routing kernel
-    int* ccnt = nullptr;        // [T][d/256] arrival counters of the combine fused into the W2 epilogue
+    int* ccnt = nullptr;        // [T][d/128] arrival counters of the combine fused into the W2 epilogue
     void* Xp = nullptr;
     void* H = nullptr;
     float* Ys = nullptr;
@@ -73,7 +73,7 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.inv = take(R * 4);
     L.sched = take(static_cast<size_t>(sched_ints(c->n)) * 4);
     L.xchg = take(static_cast<size_t>(fused_route_xchg_ints()) * 4);
-    L.ccnt = take(Tn * static_cast<size_t>((c->d + 255) / 256) * 4);
+    L.ccnt = take(Tn * static_cast<size_t>((c->d + 127) / 128) * 4);
     L.Xp = take(R * c->d * es);
     L.H = take(R * c->F * es);
     L.Ys = take(R * c->d * 4);
@@ -173,15 +173,13 @@ bool use_decode(const moe_ctx* c, int T) {
     return c->force_path == 2 || T <= c->decode_max_t;
 }
 
-// The grouped GEMMs run on single CTAs (128-row tiles) unless the caller asks
-// for CTA pairs.  Pairs move a third fewer operand bytes per FLOP and take ~10%
-// fewer cycles per launch, but their 256-row tiles pad each expert group by
-// 128 rows on average, and under the board's power cap that extra tensor work
-// costs more clock than the saved traffic gives back (measured at T=4096).
-bool use_pair(const moe_ctx* c) {
-    if (c->gemm_pair != 2) return false;
-    return pair_gemm_available(c->num_sms);
-}
+// Which grouped GEMMs run on CTA pairs.  Pairs move a third fewer operand
+// bytes per FLOP; at the Mixtral shape under the board's power cap that made
+// the W2 GEMM (K = d_ff, long tiles) ~4% faster and the W1/W3 GEMM (K = d)
+// ~4% slower than single CTAs (T = 4096, measured back to back), so by default
+// only W2 runs on pairs.
+bool use_pair13(const moe_ctx* c) { return c->gemm_pair == 2 && pair_gemm_available(c->num_sms); }
+bool use_pair2(const moe_ctx* c) { return c->gemm_pair != 1 && pair_gemm_available(c->num_sms); }
 
 // Stages of one forward call, in launch order.
 constexpr int kStages = 4;
@@ -272,16 +270,19 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         marks.finish();
         return MOE_OK;
     } else {
-        const bool pair = use_pair(c);
-        if (c->gemm_pair == 2 && !pair) return MOE_ERR_UNSUPPORTED;
+        const bool pair13 = use_pair13(c), pair2 = use_pair2(c);
+        if (c->gemm_pair == 2 && !pair13) return MOE_ERR_UNSUPPORTED;
         CUtensorMap mW1, mW3, mW2;
         const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
         if (!encode_map_bf16_2d(&mW1, W1, nF, c->d, 128) || !encode_map_bf16_2d(&mW3, W3, nF, c->d, 128) ||
-            !encode_map_bf16_2d(&mW2, W2, nd, c->F, pair ? 128 : 256))
+            !encode_map_bf16_2d(&mW2, W2, nd, c->F, pair2 ? 128 : 256))
             return MOE_ERR_CUDA;
         const KStatus st = kstatus(c);
-        if (pair)
-            e = launch_pair_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
+        CUtensorMap mW1h, mW3h;
+        if (pair13 && (!encode_map_bf16_2d(&mW1h, W1, nF, c->d, 64) || !encode_map_bf16_2d(&mW3h, W3, nF, c->d, 64)))
+            return MOE_ERR_CUDA;
+        if (pair13)
+            e = launch_pair_gemm13(c->map_Xp, mW1, mW3, mW1h, mW3h, c->sched, c->n, c->d, c->F, R,
                                    static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
         else
             e = launch_tc_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
@@ -292,9 +293,9 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         comb.cnt = c->ccnt;
         comb.y = static_cast<__nv_bfloat16*>(y);
         comb.K = c->k;
-        comb.nblk = c->d / 256;
+        comb.nblk = c->d / 128;
         comb.d = c->d;
-        if (pair)
+        if (pair2)
             e = launch_pair_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, comb, st,
                                   c->num_sms, s);
         else

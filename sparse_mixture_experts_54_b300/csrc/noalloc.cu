@@ -13,8 +13,10 @@
 // rows, the SwiGLU rows and the per-slot expert outputs -- lives in one
 // file-scope __device__ array of fixed size.  The CUDA module that holds it is
 // loaded once per device, so every GPU that loads this library keeps the
-// array until the process exits.  The kernels are the same ones moe_forward
-// launches; only where their scratch lives differs.
+// array until the process exits.  It launches the library's separate router,
+// dispatch, gather, grouped-GEMM and combine kernels (moe_forward fuses some
+// of these steps with the help of counters kept in its context's workspace),
+// so its results agree with moe_forward's within the tests' tolerance.
 #include <mutex>
 
 #include "../../include/moe.h"

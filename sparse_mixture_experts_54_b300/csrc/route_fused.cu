@@ -107,24 +107,37 @@ __device__ __forceinline__ void lane_transpose_sum(float (&v)[V], int lane) {
         }
     }
 }
-// 4 consecutive elements of a row as fp32 (zeros when !ok).
+// 4 consecutive elements of a row as loaded (bf16: 8 bytes, fp32: 16 bytes),
+// so that the next segment's loads can be in flight while one is computed.
 template <typename TX>
-__device__ __forceinline__ void load4(const TX* row, int j0, bool ok, float* v) {
-    if (!ok) {
-        v[0] = v[1] = v[2] = v[3] = 0.0f;
-        return;
-    }
+struct Raw4;
+template <>
+struct Raw4<__nv_bfloat16> {
+    uint2 v;
+};
+template <>
+struct Raw4<float> {
+    float4 v;
+};
+template <typename TX>
+__device__ __forceinline__ void load_raw4(const TX* row, int j0, bool ok, Raw4<TX>& r) {
     if constexpr (sizeof(TX) == 2) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row + j0));
-        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        r.v = ok ? __ldg(reinterpret_cast<const uint2*>(row + j0)) : make_uint2(0u, 0u);
+    } else {
+        r.v = ok ? __ldg(reinterpret_cast<const float4*>(row + j0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+template <typename TX>
+__device__ __forceinline__ void unpack_raw4(const Raw4<TX>& r, float* v) {
+    if constexpr (sizeof(TX) == 2) {
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&r.v.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&r.v.y);
         v[0] = __low2float(lo);
         v[1] = __high2float(lo);
         v[2] = __low2float(hi);
         v[3] = __high2float(hi);
     } else {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(row + j0));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[0] = r.v.x; v[1] = r.v.y; v[2] = r.v.z; v[3] = r.v.w;
     }
 }
 
@@ -192,16 +205,33 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
 #pragma unroll
             for (int e = 0; e < NMAX; ++e) acc[j][e] = 0.0f;
         const int t0 = tb + tg * TOKW;
+        // x of the first segment; inside the loop the next segment's loads are
+        // issued before the current one is used
+        Raw4<TX> rx[TOKW][2];
+#pragma unroll
+        for (int j = 0; j < TOKW; ++j) {
+            const TX* row = x + static_cast<size_t>(t0 + j) * d;
+            const bool tv = t0 + j < t_end;
+            const int j0 = q * 256 + 4 * lane;
+            load_raw4(row, j0, tv && j0 < d, rx[j][0]);
+            load_raw4(row, j0 + 128, tv && j0 + 128 < d, rx[j][1]);
+        }
         for (int sg = q; sg * 256 < d; sg += FR_DS) {
             const int j0 = sg * 256 + 4 * lane, j1 = j0 + 128;
             const bool h0 = j0 < d, h1 = j1 < d;
             float xv[TOKW][8];
 #pragma unroll
             for (int j = 0; j < TOKW; ++j) {
+                unpack_raw4(rx[j][0], &xv[j][0]);
+                unpack_raw4(rx[j][1], &xv[j][4]);
+            }
+            const int jn = j0 + FR_DS * 256;
+#pragma unroll
+            for (int j = 0; j < TOKW; ++j) {
                 const TX* row = x + static_cast<size_t>(t0 + j) * d;
                 const bool tv = t0 + j < t_end;
-                load4(row, j0, tv && h0, &xv[j][0]);
-                load4(row, j1, tv && h1, &xv[j][4]);
+                load_raw4(row, jn, tv && jn < d, rx[j][0]);
+                load_raw4(row, jn + 128, tv && jn + 128 < d, rx[j][1]);
             }
 #pragma unroll
             for (int e = 0; e < NMAX; ++e) {
@@ -371,19 +401,21 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
         if (xp4) {
             const int nr = min(FR_ROUND, a_end - a0);
             const int rv = p.row_vecs;
+            // one row per warp at a time, up to 16 x 16 bytes in flight per lane
+            // (a whole 8 KB bf16 row of the Mixtral shape)
             for (int r = warp; r < nr; r += FR_WARPS) {
                 const int2 ap = placed[r];
                 const uint4* src = xv4 + static_cast<size_t>(ap.x / K) * rv;
                 uint4* dst = xp4 + static_cast<size_t>(ap.y) * rv;
-                for (int v0 = lane; v0 < rv; v0 += 32 * 8) {
-                    uint4 buf[8];
+                for (int v0 = lane; v0 < rv; v0 += 32 * 16) {
+                    uint4 buf[16];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
+                    for (int u = 0; u < 16; ++u) {
                         const int vv = v0 + 32 * u;
                         if (vv < rv) buf[u] = __ldg(src + vv);
                     }
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
+                    for (int u = 0; u < 16; ++u) {
                         const int vv = v0 + 32 * u;
                         if (vv < rv) dst[vv] = buf[u];
                     }
