@@ -249,6 +249,9 @@ def run_ours(args, rank, world, dist):
         ms_di, stages_d = timed(xd, max(args.decode_steps // 2, 3), 0, True, clk)
     clocks = clk.summary()
 
+    # skewed, locally correlated routing at 32k context (router bias, repeated rows)
+    skew = run_skewed(args, W1, W3, W2, pk, dist) if not args.no_skewed else None
+
     # end to end: pinned host x in, host y out, through the host-buffer entry point
     xh = xp.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
@@ -303,6 +306,7 @@ def run_ours(args, rank, world, dist):
         "stages_us": {k: round(v * 1e3, 1) for k, v in stages_p.items()},
         "instrumented_ms_per_step": {"prefill": round(ms_pi, 4), "decode": round(ms_di, 4)},
         "roofline": roofline,
+        "skewed_t32768": skew,
         "e2e": {"value": round(world * wp.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                 "d2h_bytes_per_step": int(yh.numel() * yh.element_size()),
@@ -316,7 +320,108 @@ def run_ours(args, rank, world, dist):
     host = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = dict(x=xp.cpu(), Wg=Wg.cpu(), W=(W1.cpu(), W3.cpu(), W2.cpu()))
+    del xp, xd, W1, W3, W2, Wg
+    torch.cuda.empty_cache()
+    if not args.no_stack:
+        line["stack32"] = run_stack(args, dist)
     return line, host
+
+
+def run_skewed(args, W1, W3, W2, pk, dist):
+    """One layer call at T=32768 with the skewed router bias and consecutive-token
+    locality (same expert weights as the headline workload)."""
+    from sparse_mixture_experts_54_b300 import _lib, inputs
+    from sparse_mixture_experts_54_b300.layer import MoELayer
+
+    w = inputs.workload("skewed_t32768")
+    rank = int(os.environ.get("RANK", "0"))
+    x = inputs.make_x(w, "cuda", seed=rank)
+    Wg, b = inputs.make_router(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=b)
+    m.reserve(w.T)
+    r = m.route(x, Wg)
+    counts = r["counts"].cpu().tolist()
+    first = r["topk_idx"][:, 0]
+    repeat = float((first[1:] == first[:-1]).float().mean().item())
+    y = torch.empty_like(x)
+    for _ in range(2):
+        m.forward(x, Wg, W1, W3, W2, y=y)
+    steps = max(args.steps // 50, 5)
+    m.set_option(_lib.MOE_OPT_STAGE_TIMING, 1)
+    m.stage_times()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        m.forward(x, Wg, W1, W3, W2, y=y)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist)
+    stages, _ = m.stage_times()
+    assert m.status() == 0, _lib.moe_error_string(m.status())
+    m.close()
+    alg = algorithmic(w.T, counts)
+    tf = alg["flops"] / (ms * 1e-3) / 1e12
+    return {"us_per_layer": round(ms * 1e3, 1), "tokens_s": round(w.T / (ms * 1e-3), 1), "tflops": round(tf, 1),
+            "frac_of_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4),
+            "expert_loads": counts, "hot_expert_share": round(max(counts) / sum(counts), 4),
+            "first_choice_repeat_rate": round(repeat, 4), "steps": steps,
+            "stages_us": {k: round(v * 1e3, 1) for k, v in stages.items()},
+            "note": "timed with per-stage events on; router bias [1.5,0.5,0,0,0,0,-0.5,-1], row repeat p=0.5"}
+
+
+def run_stack(args, dist):
+    """The 32-layer stack (h <- h + MoE_l(RMSNorm(h)) per layer, layer l seeded
+    1000 + l; ~90 GB of expert weights resident): microseconds per layer through
+    moe_stack_forward for the decode sweep and one prefill pass."""
+    from sparse_mixture_experts_54_b300 import _lib, inputs
+    from sparse_mixture_experts_54_b300.layer import MoELayer
+
+    w = inputs.workload("decode_t32")
+    layers = []
+    for l in range(inputs.STACK_LAYERS):
+        Wg, _ = inputs.make_router(w, "cuda", seed=1000 + l)
+        layers.append((Wg,) + inputs.make_experts(w, "cuda", seed=1000 + l))
+    torch.cuda.synchronize()
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    m.reserve(inputs.STACK_PREFILL_T)
+    L = len(layers)
+
+    def per_layer_us(T, passes, force_path=0):
+        m.set_option(_lib.MOE_OPT_FORCE_PATH, force_path)
+        h0 = inputs.make_x(w, "cuda", seed=2000 + T, T=T)
+        h = h0.clone()
+        m.stack_forward(h, layers, 1e-5)   # warm-up pass
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(passes):
+            m.stack_forward(h, layers, 1e-5)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(dist)
+        assert m.status() == 0, _lib.moe_error_string(m.status())
+        return max_over_ranks(e0.elapsed_time(e1) * 1e3 / (passes * L), dist)
+
+    out = {"layers": L, "expert_weight_gbytes": round(L * 3 * w.n_experts * w.d * w.d_ff * 2 / 1e9, 2),
+           "timing": "CUDA events around whole stack passes (h updated in place; weights streamed from HBM)",
+           "decode_us_per_layer": {}, "decode_path_us_per_layer": {}}
+    for T in inputs.STACK_DECODE_T:
+        out["decode_us_per_layer"][str(T)] = round(per_layer_us(T, args.stack_passes), 1)
+        if T > 64:
+            out["decode_path_us_per_layer"][str(T)] = round(per_layer_us(T, args.stack_passes, force_path=2), 1)
+    Tp = inputs.STACK_PREFILL_T
+    us = per_layer_us(Tp, max(args.stack_passes // 4, 2))
+    out["prefill_t8192_us_per_layer"] = round(us, 1)
+    out["prefill_t8192_tokens_s_per_layer"] = round(Tp / (us * 1e-6), 1)
+    out["prefill_t8192_stack_ms"] = round(us * L / 1e3, 2)
+    m.close()
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -414,6 +519,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack measurement")
+    ap.add_argument("--no-skewed", action="store_true", help="skip the skewed T=32768 measurement")
+    ap.add_argument("--stack-passes", type=int, default=8)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=6.0)
     ap.add_argument("--profile-step", default=None, help="workload name: run warmup+1 untimed calls (for ncu)")

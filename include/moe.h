@@ -65,14 +65,16 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype_t;
 
 /* Options for moe_set_option. */
 typedef enum {
-    MOE_OPT_DECODE_MAX_T = 1,  /* forward uses the weight-streaming decode kernels when T <= value (default 64) */
+    MOE_OPT_DECODE_MAX_T = 1,  /* forward uses the weight-streaming decode kernels when T <= value (default 128) */
     MOE_OPT_WAIT_LIMIT_US = 2, /* wall-time limit of every bounded wait inside a kernel (default 2,000,000 us) */
     MOE_OPT_FORCE_PATH = 3,    /* 0 = choose by T, 1 = always grouped GEMM, 2 = always decode kernels */
     MOE_OPT_STAGE_TIMING = 4,  /* 1 = record CUDA events around every kernel of moe_forward (see moe_stage_times) */
-    MOE_OPT_GEMM_PAIR = 5      /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
+    MOE_OPT_GEMM_PAIR = 5,     /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
                                   CTA pairs -- tcgen05 cta_group::2, 256/128-row tiles -- when the device can
                                   co-schedule them), 1 = both single-CTA, 2 = both on CTA pairs or
                                   MOE_ERR_UNSUPPORTED */
+    MOE_OPT_L2_PREFETCH = 6    /* grouped GEMMs: prefetch operand tiles into L2 this many 64-wide k-steps ahead of
+                                  their loads (0 = off, the default); process-wide, not per context */
 } moe_option_t;
 
 /*
@@ -153,6 +155,33 @@ int moe_forward(moe_ctx* ctx, const void* x, const float* W_g, const void* W1, c
  */
 int moe_forward_host(moe_ctx* ctx, const void* x_host, const float* W_g, const void* W1,
                      const void* W3, const void* W2, void* y_host, int T, moe_stream_t stream);
+
+/*
+ * One residual block of a layer stack, in place:
+ *     h <- h + MoE(RMSNorm(h)),   RMSNorm(h) = h / sqrt(mean_j h_j^2 + eps)  (unit gain)
+ * The pages' block diagram has, per layer, RMSNorm -> attention -> RMSNorm ->
+ * MoE with residual connections (the DL reading-group slides, "Architecture -
+ * 全体"; 32 layers, xyznot "Method"); this is the MoE half of it (attention
+ * is outside this library).  h [T][d] (device, context dtype) is read and
+ * overwritten.  The normalised row is rounded to the element type once and
+ * feeds both the router and the experts; h + MoE(...) is summed in fp32 and
+ * rounded once.  eps >= 0 (Mixtral-style models use 1e-5).  Other arguments,
+ * errors and asynchrony as moe_forward.
+ */
+int moe_block_forward(moe_ctx* ctx, void* h, float eps, const float* W_g, const void* W1,
+                      const void* W3, const void* W2, int T, moe_stream_t stream);
+
+/*
+ * n_layers residual blocks in order (layer l uses W_g[l], W1[l], W3[l], W2[l]):
+ * for l in 0..n_layers-1: h <- h + MoE_l(RMSNorm(h)).  The four arguments are
+ * host arrays of n_layers device pointers (each layout as moe_forward).  The
+ * context's router bias, if set, applies to every layer.  Launches 3 kernels
+ * per layer for T above the decode threshold (5 at or below it); nothing is
+ * synchronised.  Returns the first error; the layers before it have run.
+ */
+int moe_stack_forward(moe_ctx* ctx, void* h, float eps, int n_layers, const float* const* W_g,
+                      const void* const* W1, const void* const* W3, const void* const* W2, int T,
+                      moe_stream_t stream);
 
 /* Sticky kernel-side status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BOUNDS) of every
  * call so far; reads host-mapped memory, synchronises nothing.  Results written

@@ -181,3 +181,55 @@ def moe_forward(x, Wg, W1, W3, W2, K: int, bias=None, toks=None, nthreads: Optio
     y = moe_tokens(x, W1, W3, W2, idx, gate, toks, nthreads)
     return dict(logits=logits, idx=idx, gate=gate, counts=counts, offsets=offsets, perm=perm,
                 y=y, toks=np.asarray(toks, dtype=np.int64))
+
+
+# ----------------------------------------------------------------------------- the residual stack
+# The pages' block diagram (DL reading-group slides, "Architecture - 全体") repeats,
+# 32 times (xyznot "Method"), RMSNorm -> attention -> RMSNorm -> MoE, each with a
+# residual connection.  The MoE half of a block, as built here:
+#     u = RMSNorm(h) = h / sqrt(mean_j h_j^2 + eps)      (unit gain; the pages only name it)
+#     h <- h + MoE(u)
+# with the hidden state h and the MoE input u stored in bf16, as the model's
+# activations are.  The oracle follows its own trajectory in fp64, rounding
+# to bf16 exactly where the definition stores a value.
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 (ties to even), directly -- no detour
+    through fp32, whose own rounding could move a value onto a bf16 tie.  Returns
+    the bit patterns (uint16).  Normal-range values only (|v| in [2^-126, 2^127))
+    or zero; that covers every activation here."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)                      # v = m * 2^e, 0.5 <= |m| < 1
+    q = np.rint(m * 256.0)                  # 8 significant bits, ties to even
+    r = np.ldexp(q / 256.0, e)              # exact: q has at most 9 bits
+    bits = np.ascontiguousarray(r.astype(np.float32)).view(np.uint32)
+    return (bits >> 16).astype(np.uint16)
+
+
+def rms_norm(h: np.ndarray, eps: float) -> np.ndarray:
+    """fp64 RMSNorm with unit gain of stored rows h [S][d] (bf16 bits or fp32)."""
+    h64 = widen(h)
+    ms = np.mean(h64 * h64, axis=1, keepdims=True)
+    return h64 / np.sqrt(ms + eps)
+
+
+def _store_like(v: np.ndarray, h: np.ndarray) -> np.ndarray:
+    """fp64 values stored in h's element type: bf16 bits (rounded to nearest even)
+    or fp32 (numpy's conversion, also to nearest even)."""
+    if h.dtype == np.uint16:
+        return round_bf16(v)
+    return v.astype(np.float32)
+
+
+def block_forward(h: np.ndarray, Wg, W1, W3, W2, K: int, eps: float, bias=None, nthreads: Optional[int] = None):
+    """One residual block on the given rows h [S][d] (bf16 bits or fp32): the MoE
+    of RMSNorm(h) stored in h's element type, added to h in fp64.
+
+    Returns dict(u=the stored MoE input, logits, idx, gate, y=MoE(u) fp64,
+    h_new=h + y in fp64 (before the storage rounding), h_bits=h_new stored)."""
+    u = _store_like(rms_norm(h, eps), h)
+    logits = router_logits(u, Wg, bias)
+    idx, gate = select_topk(logits, K)
+    y = moe_tokens(u, W1, W3, W2, idx, gate, np.arange(u.shape[0]), nthreads)
+    h_new = widen(h) + y
+    return dict(u=u, logits=logits, idx=idx, gate=gate, y=y, h_new=h_new, h_bits=_store_like(h_new, h))

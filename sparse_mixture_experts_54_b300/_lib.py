@@ -31,6 +31,7 @@ MOE_OPT_WAIT_LIMIT_US = 2
 MOE_OPT_FORCE_PATH = 3
 MOE_OPT_STAGE_TIMING = 4
 MOE_OPT_GEMM_PAIR = 5
+MOE_OPT_L2_PREFETCH = 6
 
 # Every entry point declared in include/moe.h, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -47,6 +48,8 @@ SIGNATURES = {
     "moe_router_logits": (_I, [_P, _P, _P, _I, _P, _P]),
     "moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "moe_block_forward": (_I, [_P, _P, ctypes.c_float, _P, _P, _P, _P, _I, _P]),
+    "moe_stack_forward": (_I, [_P, _P, ctypes.c_float, _I, _P, _P, _P, _P, _I, _P]),
     "moe_status": (_I, [_P]),
     "moe_clear_status": (_I, [_P]),
     "moe_selftest_wait_timeout": (_I, [_P, _LL, _P]),
@@ -138,6 +141,16 @@ def moe_forward(ctx, x, W_g, W1, W3, W2, y, T, stream) -> int:
 
 def moe_forward_host(ctx, x_host, W_g, W1, W3, W2, y_host, T, stream) -> int:
     return load().moe_forward_host(ctx, _p(x_host), _p(W_g), _p(W1), _p(W3), _p(W2), _p(y_host), T, _p(stream))
+
+
+def moe_block_forward(ctx, h, eps, W_g, W1, W3, W2, T, stream) -> int:
+    return load().moe_block_forward(ctx, _p(h), float(eps), _p(W_g), _p(W1), _p(W3), _p(W2), T, _p(stream))
+
+
+def moe_stack_forward(ctx, h, eps, n_layers, W_g, W1, W3, W2, T, stream) -> int:
+    """W_g, W1, W3, W2: addresses of host arrays of n_layers device pointers."""
+    return load().moe_stack_forward(ctx, _p(h), float(eps), n_layers, _p(W_g), _p(W1), _p(W3), _p(W2), T,
+                                    _p(stream))
 
 
 def moe_status(ctx) -> int:

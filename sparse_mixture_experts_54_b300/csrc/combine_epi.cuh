@@ -8,7 +8,8 @@
 // thread adds 1 to the counter of (token t, feature block); the thread that
 // brings it to K is the last of the token's K rows there, and its warp adds
 // the K rows in slot order (slot 0 first, then 1, ...) from L2, rounds once to
-// bf16 and writes y, then puts the counter back to 0 for the next call.  The
+// bf16 (after adding the residual row h, when given) and writes y, then puts
+// the counter back to 0 for the next call.  The
 // sum and its order are the same whichever row arrives last, so y is bitwise
 // reproducible.
 #pragma once
@@ -20,6 +21,7 @@ namespace moe {
 struct CombineArgs {
     int* cnt;               // [T][d/128] arrival counters, zero between calls (null: no fused combine)
     __nv_bfloat16* y;       // [T][d]
+    const __nv_bfloat16* resid;   // optional [T][d] added before the rounding (may be y itself)
     int K;
     int nblk;               // d / 128
     int d;
@@ -70,6 +72,22 @@ __device__ __forceinline__ void combine_arrive(const CombineArgs& c, const float
                 if (r < nr) {
                     const float4 u = ldcg_f4(Ys + (static_cast<size_t>(tt[r]) * c.K + k) * ldY + col);
                     s[r].x += u.x; s[r].y += u.y; s[r].z += u.z; s[r].w += u.w;
+                }
+            }
+        }
+#pragma unroll
+        if (c.resid) {
+            // residual stream: y = h + (sum of the slot rows), one rounding
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (r < nr) {
+                    const uint2 hv = *reinterpret_cast<const uint2*>(c.resid + static_cast<size_t>(tt[r]) * c.d + col);
+                    const __nv_bfloat162 h0 = *reinterpret_cast<const __nv_bfloat162*>(&hv.x);
+                    const __nv_bfloat162 h1 = *reinterpret_cast<const __nv_bfloat162*>(&hv.y);
+                    s[r].x = __low2float(h0) + s[r].x;
+                    s[r].y = __high2float(h0) + s[r].y;
+                    s[r].z = __low2float(h1) + s[r].z;
+                    s[r].w = __high2float(h1) + s[r].w;
                 }
             }
         }

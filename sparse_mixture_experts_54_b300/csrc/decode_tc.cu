@@ -311,11 +311,12 @@ __global__ void __launch_bounds__(256) decode_swiglu_kernel(const float4* __rest
 }
 
 // y[t][i] = sum_k g[t][k] * (sum_s P2[s][inv[t*K+k]][i]), slots in order, one rounding.
+// With resid (may be y itself): y = resid + that sum, one rounding.
 template <typename TY>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __restrict__ P2, int S, size_t part4,
                                                              const int32_t* __restrict__ inv,
                                                              const float* __restrict__ topk_w, int T, int K, int d4,
-                                                             TY* __restrict__ y) {
+                                                             const TY* resid, TY* y) {
     griddep_launch_dependents();
     griddep_wait();
     const size_t total = static_cast<size_t>(T) * d4;
@@ -333,6 +334,20 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float4* __res
                 v.x += v2.x; v.y += v2.y; v.z += v2.z; v.w += v2.w;
             }
             acc.x += g * v.x; acc.y += g * v.y; acc.z += g * v.z; acc.w += g * v.w;
+        }
+        if (resid) {
+            float r[4];
+            if constexpr (sizeof(TY) == 4) {
+                const float4 h = reinterpret_cast<const float4*>(resid)[i];
+                r[0] = h.x; r[1] = h.y; r[2] = h.z; r[3] = h.w;
+            } else {
+                const uint2 h = reinterpret_cast<const uint2*>(resid)[i];
+                r[0] = __low2float(*reinterpret_cast<const __nv_bfloat162*>(&h.x));
+                r[1] = __high2float(*reinterpret_cast<const __nv_bfloat162*>(&h.x));
+                r[2] = __low2float(*reinterpret_cast<const __nv_bfloat162*>(&h.y));
+                r[3] = __high2float(*reinterpret_cast<const __nv_bfloat162*>(&h.y));
+            }
+            acc.x = r[0] + acc.x; acc.y = r[1] + acc.y; acc.z = r[2] + acc.z; acc.w = r[3] + acc.w;
         }
         if constexpr (sizeof(TY) == 4) {
             reinterpret_cast<float4*>(y)[i] = acc;
@@ -441,7 +456,7 @@ cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R,
 }
 
 cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
-                                  int T, int K, int d, void* y, cudaStream_t s) {
+                                  int T, int K, int d, const void* resid, void* y, cudaStream_t s) {
     const size_t part4 = static_cast<size_t>(R) * d / 4;
     const int d4 = d / 4;
     const size_t total = static_cast<size_t>(T) * d4;
@@ -451,9 +466,9 @@ cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, co
     if (et == ElemType::BF16)
         return launch_pdl(decode_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
                           reinterpret_cast<const float4*>(P2), S, part4, inv, topk_w, T, K, d4,
-                          static_cast<__nv_bfloat16*>(y));
+                          static_cast<const __nv_bfloat16*>(resid), static_cast<__nv_bfloat16*>(y));
     return launch_pdl(decode_combine_kernel<float>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2),
-                      S, part4, inv, topk_w, T, K, d4, static_cast<float*>(y));
+                      S, part4, inv, topk_w, T, K, d4, static_cast<const float*>(resid), static_cast<float*>(y));
 }
 
 }  // namespace moe

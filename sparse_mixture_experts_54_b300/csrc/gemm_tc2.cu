@@ -70,6 +70,8 @@ struct PairArgs {
     int n;
     int kblocks;          // K / 64
     int ntiles;           // N blocks per expert
+    int group_m;          // 256-row blocks per tile group
+    int pf_dist;          // k-steps ahead at which the producer prefetches operand tiles into L2 (0: off)
     int b_rows_per_e;     // rows of the B tensors per expert (F for MODE 0, d for MODE 1)
     __nv_bfloat16* H;     // MODE 0 output [R][F]
     int ldH;
@@ -81,17 +83,20 @@ struct PairArgs {
     KStatus st;
 };
 
-// tile -> (expert, 256-row block, N block, 128-row tile?); expert-major, then N
-// block, then row block.
-__device__ __forceinline__ void pair_decode_tile(const int* prefix, const int* counts, int n, int ntiles, int tile,
-                                                 int& e, int& mb, int& nb, bool& half) {
+// tile -> (expert, 256-row block, N block, 128-row tile?); expert-major, then
+// groups of group_m row blocks, then N block, then row block (as in gemm_tc.cu).
+__device__ __forceinline__ void pair_decode_tile(const int* prefix, const int* counts, int n, int ntiles, int group_m,
+                                                 int tile, int& e, int& mb, int& nb, bool& half) {
     int k = 0;
     while (k + 1 < n && prefix[k + 1] * ntiles <= tile) ++k;
     const int mt = prefix[k + 1] - prefix[k];
     const int local = tile - prefix[k] * ntiles;
+    const int g = local / (group_m * ntiles);   // row-block groups, as in tc_decode_tile
+    const int mg = min(group_m, mt - g * group_m);
+    const int r = local - g * group_m * ntiles;
     e = k;
-    nb = local / mt;
-    mb = local % mt;
+    nb = r / mg;
+    mb = g * group_m + r % mg;
     const int rem = counts[k] - mb * Q_PAIR_ROWS;   // rows of the group from this tile on
     half = rem <= 128;
 }
@@ -186,16 +191,46 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // this CTA's A and B rows for a tile
+            auto tile_rows = [&](int t, int& ar, int& br, bool& hf) {
+                int e2, mb2, nb2;
+                pair_decode_tile(prefix, counts, n, p.ntiles, p.group_m, t, e2, mb2, nb2, hf);
+                ar = offsets[e2] + mb2 * Q_PAIR_ROWS + static_cast<int>(rank) * (hf ? 64 : 128);
+                br = e2 * p.b_rows_per_e +
+                     (MODE == 0 ? nb2 * 128 + (hf ? 64 * static_cast<int>(rank) : 0)
+                                : nb2 * 256 + static_cast<int>(rank) * 128);
+            };
+            // L2 prefetch of the tiles pf_dist k-steps ahead (whole 128-row boxes)
+            auto prefetch = [&](int ar, int br, bool hf, int kb) {
+                tma_prefetch_l2_2d(&tmA, kb * Q_BK, ar);
+                if (MODE == 0 && hf) {
+                    tma_prefetch_l2_2d(&tmB0h, kb * Q_BK, br);
+                    tma_prefetch_l2_2d(&tmB1h, kb * Q_BK, br);
+                } else {
+                    tma_prefetch_l2_2d(mapB, kb * Q_BK, br);
+                }
+            };
+            const int pf = p.pf_dist < p.kblocks ? p.pf_dist : p.kblocks;
+            if (pf > 0 && cid < total) {
+                int ar, br;
+                bool hf;
+                tile_rows(cid, ar, br, hf);
+                for (int kb = 0; kb < pf; ++kb) prefetch(ar, br, hf, kb);
+            }
             for (int tile = cid; tile < total && ok; tile += ncl) {
-                int e, mb, nb;
+                int arow, brow;
                 bool half;
-                pair_decode_tile(prefix, counts, n, p.ntiles, tile, e, mb, nb, half);
-                // A: this CTA's 128 rows (a 128-row tile uses the first 64 of them)
-                const int arow = offsets[e] + mb * Q_PAIR_ROWS + static_cast<int>(rank) * (half ? 64 : 128);
-                const int brow = e * p.b_rows_per_e +
-                                 (MODE == 0 ? nb * 128 + (half ? 64 * static_cast<int>(rank) : 0)
-                                            : nb * 256 + static_cast<int>(rank) * 128);
+                tile_rows(tile, arow, brow, half);
+                int next_ar = 0, next_br = 0;
+                bool next_half = false;
+                const bool has_next = tile + ncl < total;
+                if (pf > 0 && has_next) tile_rows(tile + ncl, next_ar, next_br, next_half);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (pf > 0) {
+                        const int kp = kb + pf;
+                        if (kp < p.kblocks) prefetch(arow, brow, half, kp);
+                        else if (has_next) prefetch(next_ar, next_br, next_half, kp - p.kblocks);
+                    }
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
                     const uint32_t a_dst = tiles_u32 + stage * Q_STAGE_BYTES;
                     const uint32_t b_dst = a_dst + Q_A_BYTES;
@@ -241,7 +276,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             for (int tile = cid; tile < total && ok; tile += ncl) {
                 int e, mb, nb;
                 bool half;
-                pair_decode_tile(prefix, counts, n, p.ntiles, tile, e, mb, nb, half);
+                pair_decode_tile(prefix, counts, n, p.ntiles, p.group_m, tile, e, mb, nb, half);
                 const uint32_t idesc = half ? idesc_half : idesc_full;
                 if (!mbar_wait_cluster(acce_bar(acc), acc_phase ^ 1u, st, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -282,7 +317,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
         for (int tile = cid; tile < total; tile += ncl) {
             int e, mb, nb;
             bool half;
-            pair_decode_tile(prefix, counts, n, p.ntiles, tile, e, mb, nb, half);
+            pair_decode_tile(prefix, counts, n, p.ntiles, p.group_m, tile, e, mb, nb, half);
             if (!mbar_wait_cluster(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
             // Full tile: lane L of this CTA's tensor memory is tile row 128*rank + L,
@@ -417,6 +452,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
                         const CUtensorMap& b1h, PairArgs args, int num_sms, cudaStream_t s) {
     const int nc = pair_clusters<MODE>(num_sms);
     if (nc <= 0) return cudaErrorNotSupported;
+    args.pf_dist = gemm_l2_prefetch_distance();
     auto kern = tc_pair_gemm_kernel<MODE>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * nc);
@@ -448,6 +484,7 @@ cudaError_t launch_pair_gemm13(const CUtensorMap& mapXp, const CUtensorMap& mapW
     args.n = n;
     args.kblocks = d / Q_BK;
     args.ntiles = F / 128;
+    args.group_m = tile_group_rows(Q_PAIR_ROWS, d);
     args.b_rows_per_e = F;
     args.H = H;
     args.ldH = F;
@@ -465,6 +502,7 @@ cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_
     args.n = n;
     args.kblocks = F / Q_BK;
     args.ntiles = d / 256;
+    args.group_m = tile_group_rows(Q_PAIR_ROWS, F);
     args.b_rows_per_e = d;
     args.Ys = Ys;
     args.ldY = d;

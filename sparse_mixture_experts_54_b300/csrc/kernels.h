@@ -21,6 +21,19 @@ inline int sched_ints(int n) { return 3 * n + 2; }
 
 enum class ElemType { BF16 = 0, F32 = 1 };
 
+// Row blocks per tile group of the grouped GEMMs: as many as keep the group's A
+// rows (rows x k_elems bf16 each) within 96 MB, most of the 126 MB L2.
+inline int tile_group_rows(int rows_per_block, int k_elems) {
+    const long long bytes = static_cast<long long>(rows_per_block) * k_elems * 2;
+    const long long g = (96ll << 20) / (bytes > 0 ? bytes : 1);
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+
+// k-steps ahead at which the grouped GEMMs' producers prefetch operand tiles
+// into L2 (0 = off); process-wide, set through MOE_OPT_L2_PREFETCH.
+int gemm_l2_prefetch_distance();
+void set_gemm_l2_prefetch_distance(int k_steps);
+
 // Launch with programmatic stream serialisation (see griddep_wait).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
@@ -46,17 +59,21 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int R, int n, int* sched, i
                             int32_t* inv, KStatus st, cudaStream_t s);
 cudaError_t launch_gather(ElemType et, const void* x, const int32_t* perm, int R, int K, int d,
                           void* Xp, cudaStream_t s);
-cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, void* y, cudaStream_t s);
+// resid: optional [T][d] (may be y) added to the slot sum before the rounding.
+cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, const void* resid, void* y,
+                           cudaStream_t s);
 
 // Router + top-k + dispatch + row gather in one kernel (route_fused.cu).  xchg
 // holds fused_route_xchg_ints() ints that must be zero before the first call;
 // every complete call leaves them as it found them.  Xp and logits may be null.
+// rstd non-null ([T] floats): RMSNorm the rows first (eps = norm_eps).
 constexpr int kFusedRouteMaxBlocks = 160;
 inline int fused_route_xchg_ints() { return 2 + kFusedRouteMaxBlocks * 32; }
 int fused_route_blocks(int T, int num_sms);
 cudaError_t launch_fused_route(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d, int n,
                                int K, int32_t* topk_idx, float* topk_w, float* logits, int* sched, int32_t* perm,
-                               int32_t* inv, void* Xp, int* xchg, KStatus st, int num_sms, cudaStream_t s);
+                               int32_t* inv, void* Xp, int* xchg, float norm_eps, float* rstd, KStatus st,
+                               int num_sms, cudaStream_t s);
 
 // CUDA-core grouped GEMMs (fp32 path) ------------------------------------------
 cudaError_t launch_simt_gemm13(ElemType et, const void* Xp, const void* W1, const void* W3, void* H,
@@ -98,7 +115,7 @@ cudaError_t launch_decode_w2(const CUtensorMap& mapW2_128, const CUtensorMap& ma
 cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R, int F, __nv_bfloat16* H,
                                  cudaStream_t s);
 cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
-                                  int T, int K, int d, void* y, cudaStream_t s);
+                                  int T, int K, int d, const void* resid, void* y, cudaStream_t s);
 
 // self-test of the bounded waits -------------------------------------------------
 cudaError_t launch_wait_selftest(KStatus st, cudaStream_t s);

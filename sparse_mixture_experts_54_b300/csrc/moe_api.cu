@@ -15,7 +15,7 @@ struct moe_ctx {
     int d = 0, F = 0, n = 0, k = 0;
     int dtype = MOE_BF16;
     const float* bias = nullptr;
-    int decode_max_t = 64;
+    int decode_max_t = 128;     // weight streaming beats the grouped GEMMs up to here (T=128: 516 vs 534 us/layer)
     long long wait_limit_us = 2000000;
     int force_path = 0;
     int gemm_pair = 0;          // 0 auto, 1 single CTA, 2 CTA pairs
@@ -35,6 +35,7 @@ struct moe_ctx {
     int* sched = nullptr;
     int* xchg = nullptr;        // grid-barrier words and block counts of the fused routing kernel
     int* ccnt = nullptr;        // [T][d/128] arrival counters of the combine fused into the W2 epilogue
+    float* rstd = nullptr;      // [T] 1/rms of each row (residual blocks: RMSNorm before routing)
     void* Xp = nullptr;
     void* H = nullptr;
     float* Ys = nullptr;
@@ -57,7 +58,7 @@ size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, Xp, H, Ys, xbuf, ybuf, Pa, Pb, P2, total;
+    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, rstd, Xp, H, Ys, xbuf, ybuf, Pa, Pb, P2, total;
 };
 
 Layout layout_for(const moe_ctx* c, int T, int Tdec) {
@@ -74,6 +75,7 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.sched = take(static_cast<size_t>(sched_ints(c->n)) * 4);
     L.xchg = take(static_cast<size_t>(fused_route_xchg_ints()) * 4);
     L.ccnt = take(Tn * static_cast<size_t>((c->d + 127) / 128) * 4);
+    L.rstd = take(Tn * 4);
     L.Xp = take(R * c->d * es);
     L.H = take(R * c->F * es);
     L.Ys = take(R * c->d * 4);
@@ -141,6 +143,7 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->sched = reinterpret_cast<int*>(b + L.sched);
     c->xchg = reinterpret_cast<int*>(b + L.xchg);
     c->ccnt = reinterpret_cast<int*>(b + L.ccnt);
+    c->rstd = reinterpret_cast<float*>(b + L.rstd);
     c->Xp = b + L.Xp;
     c->H = b + L.H;
     c->Ys = reinterpret_cast<float*>(b + L.Ys);
@@ -151,7 +154,7 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->P2 = reinterpret_cast<float*>(b + L.P2);
     c->cap_T = T;
     c->cap_dec = Tdec;
-    if (cudaMemsetAsync(c->xchg, 0, L.Xp - L.xchg, s) != cudaSuccess) return MOE_ERR_CUDA;   // xchg + ccnt
+    if (cudaMemsetAsync(c->xchg, 0, L.rstd - L.xchg, s) != cudaSuccess) return MOE_ERR_CUDA;   // xchg + ccnt
     // Tensor maps of the workspace activations cover the full capacity; rows
     // beyond the live K*T are never valid rows of any tile.
     if (c->dtype == MOE_BF16) {
@@ -220,21 +223,25 @@ struct StageMarks {
     }
 };
 
-// router + top-k + dispatch (+ the row gather into Xp when gather is set)
-int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s, float* logits, bool gather) {
+// router + top-k + dispatch (+ the row gather into Xp when gather is set);
+// norm_eps >= 0: RMSNorm the rows first
+int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s, float* logits, bool gather,
+              float norm_eps = -1.0f) {
     const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
     cudaError_t e = launch_fused_route(et, x, Wg, c->bias, T, c->d, c->n, c->k, c->topk_idx, c->topk_w, logits,
-                                       c->sched, c->perm, c->inv, gather ? c->Xp : nullptr, c->xchg, kstatus(c),
-                                       c->num_sms, s);
+                                       c->sched, c->perm, c->inv, gather ? c->Xp : nullptr, c->xchg,
+                                       norm_eps, norm_eps >= 0.0f ? c->rstd : nullptr, kstatus(c), c->num_sms, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+// y = MoE(x); with norm_eps >= 0 and resid: y = resid + MoE(RMSNorm(x)) (the
+// residual block of a stack, x == resid == y allowed).
 int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
-                int T, cudaStream_t s) {
+                int T, cudaStream_t s, float norm_eps = -1.0f, const void* resid = nullptr) {
     const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
     const int R = c->k * T;
     StageMarks marks(c, s);
-    int rc = run_route(c, x, Wg, T, s, nullptr, true);
+    int rc = run_route(c, x, Wg, T, s, nullptr, true, norm_eps);
     if (rc != MOE_OK) return rc;
     marks.mark(0);
     cudaError_t e = cudaSuccess;
@@ -264,7 +271,7 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         e = launch_decode_w2(mW2, c->map_H32, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.mark(2);
-        e = launch_decode_combine(et, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, y, s);
+        e = launch_decode_combine(et, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, resid, y, s);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.mark(3);
         marks.finish();
@@ -292,6 +299,7 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         CombineArgs comb{};
         comb.cnt = c->ccnt;
         comb.y = static_cast<__nv_bfloat16*>(y);
+        comb.resid = static_cast<const __nv_bfloat16*>(resid);
         comb.K = c->k;
         comb.nblk = c->d / 128;
         comb.d = c->d;
@@ -307,7 +315,7 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         marks.finish();
         return MOE_OK;
     }
-    e = launch_combine(et, c->Ys, T, c->k, c->d, y, s);
+    e = launch_combine(et, c->Ys, T, c->k, c->d, resid, y, s);
     if (e != cudaSuccess) return cuda_fail(e);
     marks.mark(3);
     marks.finish();
@@ -384,6 +392,10 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
         case MOE_OPT_FORCE_PATH:
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
             c->force_path = static_cast<int>(value);
+            return MOE_OK;
+        case MOE_OPT_L2_PREFETCH:
+            if (value < 0 || value > 1024) return MOE_ERR_INVALID;
+            set_gemm_l2_prefetch_distance(static_cast<int>(value));
             return MOE_OK;
         case MOE_OPT_GEMM_PAIR:
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
@@ -462,6 +474,37 @@ int moe_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
     return run_forward(c, x, Wg, W1, W3, W2, y, T, s);
 }
 
+int moe_block_forward(moe_ctx* c, void* h, float eps, const float* Wg, const void* W1, const void* W3,
+                      const void* W2, int T, moe_stream_t stream) {
+    if (!c || T < 0 || !(eps >= 0.0f)) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    if (!h || !Wg || !W1 || !W3 || !W2) return MOE_ERR_INVALID;
+    if (!aligned16(h) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2)) return MOE_ERR_INVALID;
+    if (c->dtype == MOE_BF16 && !tc_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = ensure_workspace(c, T, s, use_decode(c, T));
+    if (rc != MOE_OK) return rc;
+    return run_forward(c, h, Wg, W1, W3, W2, h, T, s, eps, h);
+}
+
+int moe_stack_forward(moe_ctx* c, void* h, float eps, int n_layers, const float* const* Wg, const void* const* W1,
+                      const void* const* W3, const void* const* W2, int T, moe_stream_t stream) {
+    if (!c || T < 0 || n_layers < 0 || !(eps >= 0.0f)) return MOE_ERR_INVALID;
+    if (T == 0 || n_layers == 0) return MOE_OK;
+    if (!h || !Wg || !W1 || !W3 || !W2) return MOE_ERR_INVALID;
+    for (int l = 0; l < n_layers; ++l) {
+        if (!Wg[l] || !W1[l] || !W3[l] || !W2[l]) return MOE_ERR_INVALID;
+        if (!aligned16(Wg[l]) || !aligned16(W1[l]) || !aligned16(W3[l]) || !aligned16(W2[l])) return MOE_ERR_INVALID;
+    }
+    if (!aligned16(h)) return MOE_ERR_INVALID;
+    if (c->dtype == MOE_BF16 && !tc_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = ensure_workspace(c, T, s, use_decode(c, T));
+    if (rc != MOE_OK) return rc;
+    for (int l = 0; l < n_layers && rc == MOE_OK; ++l) rc = run_forward(c, h, Wg[l], W1[l], W3[l], W2[l], h, T, s, eps, h);
+    return rc;
+}
+
 int moe_forward_host(moe_ctx* c, const void* x_host, const float* Wg, const void* W1, const void* W3, const void* W2,
                      void* y_host, int T, moe_stream_t stream) {
     if (!c || T < 0) return MOE_ERR_INVALID;
@@ -495,7 +538,7 @@ int moe_clear_status(moe_ctx* c) {
     // them back (synchronously, on the device of the context).
     if (c->xchg && (*reinterpret_cast<volatile int*>(c->status_host) & kStatusTimeout)) {
         if (cudaDeviceSynchronize() != cudaSuccess ||
-            cudaMemset(c->xchg, 0, static_cast<size_t>(reinterpret_cast<char*>(c->Xp) - reinterpret_cast<char*>(c->xchg))) !=
+            cudaMemset(c->xchg, 0, static_cast<size_t>(reinterpret_cast<char*>(c->rstd) - reinterpret_cast<char*>(c->xchg))) !=
                 cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_CUDA;

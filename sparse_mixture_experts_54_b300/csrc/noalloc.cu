@@ -137,7 +137,7 @@ extern "C" int moe_forward_noalloc(const void* x, const float* W_g, const float*
                                     sms, s);
         }
     }
-    if (e == cudaSuccess) e = launch_combine(et, Ys, T, k, d, y, s);
+    if (e == cudaSuccess) e = launch_combine(et, Ys, T, k, d, nullptr, y, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;

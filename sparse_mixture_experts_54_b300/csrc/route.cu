@@ -352,9 +352,10 @@ cudaError_t launch_gather(ElemType et, const void* x, const int32_t* perm, int R
 // ---------------------------------------------------------------------------
 // Combine: y[t][i] = sum_{k=0}^{K-1} Ys[t*K+k][i], added in slot order in fp32
 // and rounded once to the output type.  Ys rows already carry the gate weight.
+// With resid (may be y itself): y = resid + the slot sum, one rounding.
 template <typename TY>
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Ys, int T, int K, int d4,
-                                                      TY* __restrict__ y) {
+                                                      const TY* resid, TY* y) {
     griddep_launch_dependents();
     griddep_wait();
     const size_t total = static_cast<size_t>(T) * d4;
@@ -367,6 +368,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
             float4 b = __ldg(src + static_cast<size_t>(k) * d4);
             a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
         }
+        if (resid) {
+            float r[4];
+            if constexpr (sizeof(TY) == 4) {
+                const float4 h = reinterpret_cast<const float4*>(resid)[i];
+                r[0] = h.x; r[1] = h.y; r[2] = h.z; r[3] = h.w;
+            } else {
+                const uint2 h = reinterpret_cast<const uint2*>(resid)[i];
+                r[0] = __low2float(*reinterpret_cast<const __nv_bfloat162*>(&h.x));
+                r[1] = __high2float(*reinterpret_cast<const __nv_bfloat162*>(&h.x));
+                r[2] = __low2float(*reinterpret_cast<const __nv_bfloat162*>(&h.y));
+                r[3] = __high2float(*reinterpret_cast<const __nv_bfloat162*>(&h.y));
+            }
+            a.x = r[0] + a.x; a.y = r[1] + a.y; a.z = r[2] + a.z; a.w = r[3] + a.w;
+        }
         if constexpr (sizeof(TY) == 4) {
             reinterpret_cast<float4*>(y)[i] = a;
         } else {
@@ -378,7 +393,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     }
 }
 
-cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, void* y, cudaStream_t s) {
+cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, const void* resid, void* y,
+                           cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int d4 = d / 4;
     const size_t total = static_cast<size_t>(T) * d4;
@@ -386,9 +402,10 @@ cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, vo
     if (blocks > 148 * 16) blocks = 148 * 16;
     if (et == ElemType::BF16)
         return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
-                          reinterpret_cast<const float4*>(Ys), T, K, d4, static_cast<__nv_bfloat16*>(y));
+                          reinterpret_cast<const float4*>(Ys), T, K, d4, static_cast<const __nv_bfloat16*>(resid),
+                          static_cast<__nv_bfloat16*>(y));
     return launch_pdl(combine_kernel<float>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(Ys), T, K,
-                      d4, static_cast<float*>(y));
+                      d4, static_cast<const float*>(resid), static_cast<float*>(y));
 }
 
 // ---------------------------------------------------------------------------

@@ -31,6 +31,13 @@
 // and the 4 quarter sums are added in q order before the bias.  The same
 // arithmetic serves moe_route, moe_router_logits and moe_forward.
 //
+// Optional RMSNorm of the rows (the residual blocks of a stack,
+// h <- h + MoE(RMSNorm(h))): with NORM the kernel first sums each row's squares
+// (fp32, in the same fixed lane/segment/quarter order), takes
+// rstd = 1 / sqrt(mean + eps), and every later use of the row -- the router's
+// dot products and the gathered expert rows -- sees x = h * rstd rounded to the
+// element type, so router and experts get the same values.
+//
 // The grid barrier: a count and a generation word in the context workspace.
 // Each block reads the generation, adds 1 to the count; the last arrival
 // resets the count to 0 and advances the generation, the others wait for it
@@ -77,8 +84,17 @@ struct FusedRouteArgs {
     int row_vecs;           // 16-byte vectors per row of x
     int* xchg;              // [0] count, [1] generation, [2 + 32*b + e] block counts
     size_t red_off;         // byte offset of the lane-sum buffer in dynamic shared memory
+    float norm_eps;         // NORM: RMSNorm epsilon
+    float* rstd;            // NORM: [T] 1 / rms of each row, for the gather
     KStatus st;
 };
+
+// x * s rounded to the element type (bf16: round to nearest even; fp32: as is).
+template <typename TX>
+__device__ __forceinline__ float scale_round(float x, float s) {
+    if constexpr (sizeof(TX) == 2) return __bfloat162float(__float2bfloat16_rn(x * s));
+    return x * s;
+}
 
 // Sum over the 32 lanes of V values per lane (V a power of two).  Each step
 // trades half of the values with the partner lane and adds, halving the count,
@@ -141,6 +157,24 @@ __device__ __forceinline__ void unpack_raw4(const Raw4<TX>& r, float* v) {
     }
 }
 
+// 16 bytes of a row (8 bf16 or 4 fp32), each element times s, rounded back.
+template <typename TX>
+__device__ __forceinline__ uint4 scale_row_vec(uint4 v, float s) {
+    if constexpr (sizeof(TX) == 2) {
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+            const __nv_bfloat162 o = __floats2bfloat162_rn(__low2float(b) * s, __high2float(b) * s);
+            w[i] = *reinterpret_cast<const uint32_t*>(&o);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        return make_uint4(__float_as_uint(__uint_as_float(v.x) * s), __float_as_uint(__uint_as_float(v.y) * s),
+                          __float_as_uint(__uint_as_float(v.z) * s), __float_as_uint(__uint_as_float(v.w) * s));
+    }
+}
+
 template <int V>
 __device__ __forceinline__ int fr_index(int lane, int i) {
     int idx = i, cur = V;
@@ -154,7 +188,7 @@ __device__ __forceinline__ int fr_index(int lane, int i) {
     return idx;
 }
 
-template <typename TX, int NMAX, int TOKW>
+template <typename TX, int NMAX, int TOKW, bool NORM>
 __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteArgs p) {
     extern __shared__ __align__(16) unsigned char fr_smem[];
     float* wg_s = reinterpret_cast<float*>(fr_smem);
@@ -162,6 +196,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     __shared__ int s_hist[32], s_cnt[32], s_pre[32], s_base[32], s_run[32];
     __shared__ int wtab[FR_WARPS][33];
     __shared__ int s_ok;
+    __shared__ float s_ss[FR_TG * TOKW][FR_DS];   // NORM: quarter sums of squares
     constexpr int TPB = FR_TG * TOKW;   // tokens per block iteration
     constexpr int V = TOKW * NMAX;
 
@@ -205,6 +240,47 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
 #pragma unroll
             for (int e = 0; e < NMAX; ++e) acc[j][e] = 0.0f;
         const int t0 = tb + tg * TOKW;
+        float rs[TOKW];
+#pragma unroll
+        for (int j = 0; j < TOKW; ++j) rs[j] = 1.0f;
+        if constexpr (NORM) {
+            // sum of squares of this warp's quarter of each row, then over lanes
+            // (butterfly) and quarters (in q order)
+            float ss[TOKW];
+#pragma unroll
+            for (int j = 0; j < TOKW; ++j) ss[j] = 0.0f;
+            for (int sg = q; sg * 256 < d; sg += FR_DS) {
+                const int j0 = sg * 256 + 4 * lane;
+#pragma unroll
+                for (int j = 0; j < TOKW; ++j) {
+                    const TX* row = x + static_cast<size_t>(t0 + j) * d;
+                    const bool tv = t0 + j < t_end;
+                    Raw4<TX> r0, r1;
+                    load_raw4(row, j0, tv && j0 < d, r0);
+                    load_raw4(row, j0 + 128, tv && j0 + 128 < d, r1);
+                    float u[8];
+                    unpack_raw4(r0, &u[0]);
+                    unpack_raw4(r1, &u[4]);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) ss[j] = fmaf(u[k], u[k], ss[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < TOKW; ++j) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], off);
+                if (lane == 0) s_ss[tg * TOKW + j][q] = ss[j];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < TOKW; ++j) {
+                float tot = 0.0f;
+#pragma unroll
+                for (int qq = 0; qq < FR_DS; ++qq) tot += s_ss[tg * TOKW + j][qq];
+                rs[j] = 1.0f / sqrtf(tot / static_cast<float>(d) + p.norm_eps);
+                if (q == 0 && lane == 0 && t0 + j < t_end) p.rstd[t0 + j] = rs[j];
+            }
+        }
         // x of the first segment; inside the loop the next segment's loads are
         // issued before the current one is used
         Raw4<TX> rx[TOKW][2];
@@ -224,6 +300,10 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
             for (int j = 0; j < TOKW; ++j) {
                 unpack_raw4(rx[j][0], &xv[j][0]);
                 unpack_raw4(rx[j][1], &xv[j][4]);
+                if constexpr (NORM) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) xv[j][k] = scale_round<TX>(xv[j][k], rs[j]);
+                }
             }
             const int jn = j0 + FR_DS * 256;
 #pragma unroll
@@ -405,14 +485,21 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
             // (a whole 8 KB bf16 row of the Mixtral shape)
             for (int r = warp; r < nr; r += FR_WARPS) {
                 const int2 ap = placed[r];
-                const uint4* src = xv4 + static_cast<size_t>(ap.x / K) * rv;
+                const int t = ap.x / K;
+                const uint4* src = xv4 + static_cast<size_t>(t) * rv;
                 uint4* dst = xp4 + static_cast<size_t>(ap.y) * rv;
+                float rsv = 1.0f;
+                if constexpr (NORM) rsv = p.rstd[t];   // written by this block in phase 1
                 for (int v0 = lane; v0 < rv; v0 += 32 * 16) {
                     uint4 buf[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int vv = v0 + 32 * u;
                         if (vv < rv) buf[u] = __ldg(src + vv);
+                    }
+                    if constexpr (NORM) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) buf[u] = scale_row_vec<TX>(buf[u], rsv);
                     }
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
@@ -437,8 +524,8 @@ int fused_route_blocks(int T, int num_sms) {
     return (T + chunk - 1) / chunk;
 }
 
-template <typename TX, int NMAX, int TOKW>
-static cudaError_t launch_fused_t(FusedRouteArgs& a, int G, cudaStream_t s) {
+template <typename TX, int NMAX, int TOKW, bool NORM>
+static cudaError_t launch_fused_n(FusedRouteArgs& a, int G, cudaStream_t s) {
     constexpr int TPB = FR_TG * TOKW;
     const size_t wg_bytes = static_cast<size_t>(a.n) * a.d * 4;
     const size_t p2_bytes = FR_ROUND * sizeof(int2);
@@ -446,15 +533,22 @@ static cudaError_t launch_fused_t(FusedRouteArgs& a, int G, cudaStream_t s) {
     base = (base + 15) & ~static_cast<size_t>(15);
     a.red_off = base;
     const size_t smem = base + static_cast<size_t>(FR_DS) * TPB * NMAX * 4;
-    auto kern = route_fused_kernel<TX, NMAX, TOKW>;
+    auto kern = route_fused_kernel<TX, NMAX, TOKW, NORM>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(G), dim3(FR_THREADS), smem, s, a);
 }
 
+template <typename TX, int NMAX, int TOKW>
+static cudaError_t launch_fused_t(FusedRouteArgs& a, int G, cudaStream_t s) {
+    if (a.rstd) return launch_fused_n<TX, NMAX, TOKW, true>(a, G, s);
+    return launch_fused_n<TX, NMAX, TOKW, false>(a, G, s);
+}
+
 cudaError_t launch_fused_route(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d, int n,
                                int K, int32_t* topk_idx, float* topk_w, float* logits, int* sched, int32_t* perm,
-                               int32_t* inv, void* Xp, int* xchg, KStatus st, int num_sms, cudaStream_t s) {
+                               int32_t* inv, void* Xp, int* xchg, float norm_eps, float* rstd, KStatus st,
+                               int num_sms, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     if (n > 32) return cudaErrorInvalidValue;
     const int G = fused_route_blocks(T, num_sms);
@@ -476,6 +570,8 @@ cudaError_t launch_fused_route(ElemType et, const void* x, const float* Wg, cons
     a.Xp = Xp;
     a.row_vecs = d * (et == ElemType::BF16 ? 2 : 4) / 16;
     a.xchg = xchg;
+    a.norm_eps = norm_eps;
+    a.rstd = rstd;
     a.st = st;
     if (et == ElemType::BF16) {
         if (n <= 8) return launch_fused_t<__nv_bfloat16, 8, 4>(a, G, s);

@@ -106,6 +106,31 @@ class MoELayer:
                                          _stream_handle(stream)), "moe_forward_host")
         return y_host
 
+    def block_forward(self, h: torch.Tensor, Wg, W1, W3, W2, eps: float = 1e-5, stream=None) -> torch.Tensor:
+        """In place: h <- h + MoE(RMSNorm(h)) (one residual block of a stack)."""
+        T = h.shape[0]
+        _lib.check(_lib.moe_block_forward(self.ctx, _dev_ptr(h, self.dtype, "h"), float(eps),
+                                          _dev_ptr(Wg, torch.float32, "W_g"), _dev_ptr(W1, self.dtype, "W1"),
+                                          _dev_ptr(W3, self.dtype, "W3"), _dev_ptr(W2, self.dtype, "W2"), T,
+                                          _stream_handle(stream)), "moe_block_forward")
+        return h
+
+    def stack_forward(self, h: torch.Tensor, layers, eps: float = 1e-5, stream=None) -> torch.Tensor:
+        """In place over the layers in order; ``layers`` is a sequence of (W_g, W1, W3, W2)."""
+        import ctypes
+        L = len(layers)
+        arrs = [(ctypes.c_void_p * max(L, 1))() for _ in range(4)]
+        for l, (Wg, W1, W3, W2) in enumerate(layers):
+            arrs[0][l] = _dev_ptr(Wg, torch.float32, "W_g")
+            arrs[1][l] = _dev_ptr(W1, self.dtype, "W1")
+            arrs[2][l] = _dev_ptr(W3, self.dtype, "W3")
+            arrs[3][l] = _dev_ptr(W2, self.dtype, "W2")
+        T = h.shape[0]
+        _lib.check(_lib.moe_stack_forward(self.ctx, _dev_ptr(h, self.dtype, "h"), float(eps), L,
+                                          *(ctypes.addressof(a) for a in arrs), T, _stream_handle(stream)),
+                   "moe_stack_forward")
+        return h
+
     def stage_times(self) -> tuple:
         """(dict stage -> mean ms per call, calls) for calls made with MOE_OPT_STAGE_TIMING on."""
         import ctypes

@@ -72,3 +72,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.load()
+
+
+def test_binding_wraps_every_entry_point():
+    # the Python binding has a same-named function for every declared entry point
+    for name in declared_functions():
+        assert callable(getattr(_lib, name, None)), f"_lib.{name} missing"

@@ -319,3 +319,72 @@ def test_threads_do_not_change_results():
     a = oracle.moe_forward(x, Wg, W1, W3, W2, 2, nthreads=1)["y"]
     b = oracle.moe_forward(x, Wg, W1, W3, W2, 2, nthreads=4)["y"]
     assert np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------- residual stack
+def tobf_bits(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    # For values that are exact in fp32, rounding straight to bf16 is what torch's
+    # fp32 -> bf16 conversion does (round to nearest, ties to even).
+    rng = np.random.default_rng(11)
+    v = np.concatenate([rng.standard_normal(20000) * s for s in (1e-3, 1.0, 37.0)]).astype(np.float32)
+    assert np.array_equal(oracle.round_bf16(v.astype(np.float64)), tobf_bits(v))
+
+
+def test_round_bf16_closed_forms():
+    # bf16 keeps 8 significant bits: between 1 and 2 the spacing is 2^-7.
+    cases = {
+        1.0: 0x3F80,
+        1.0 + 2.0 ** -8: 0x3F80,                 # exact tie -> even (1.0)
+        1.0 + 3 * 2.0 ** -8: 0x3F82,             # exact tie -> even (1 + 2^-6)
+        1.0 + 2.0 ** -8 + 2.0 ** -30: 0x3F81,    # just above the tie -> up; an fp32 detour would give 1.0
+        -2.5: 0xC020,
+        0.0: 0x0000,
+    }
+    got = oracle.round_bf16(np.array(list(cases.keys())))
+    assert [int(g) for g in got] == list(cases.values())
+
+
+def test_rms_norm_hand_worked():
+    # rows [3, 4]: mean square 12.5 -> [3, 4] / sqrt(12.5 + eps); a constant row c -> 1/sqrt(1 + eps/c^2)
+    eps = 1e-5
+    h = f32([[3.0, 4.0], [2.0, 2.0]])
+    u = oracle.rms_norm(h, eps)
+    assert np.allclose(u[0], np.array([3.0, 4.0]) / math.sqrt(12.5 + eps), rtol=0, atol=1e-15)
+    assert np.allclose(u[1], 1.0 / math.sqrt(1.0 + eps / 4.0), rtol=0, atol=1e-15)
+    # scale invariance (up to eps): RMSNorm(5h) == RMSNorm(h) when eps = 0
+    assert np.allclose(oracle.rms_norm(f32([[3.0, 4.0]]) * 5, 0.0), oracle.rms_norm(f32([[3.0, 4.0]]), 0.0),
+                       rtol=0, atol=1e-15)
+
+
+def test_block_is_residual_plus_dense_masked_moe_of_rounded_norm():
+    # h_new = h + sum_i G(u)_i E_i(u), u = bf16(h / rms(h)): brute force over all experts in numpy.
+    rng = np.random.default_rng(12)
+    T, d, F, n, K, eps = 9, 8, 12, 8, 2, 1e-5
+    _, Wg, W1, W3, W2 = rand_layer(rng, T, d, F, n, bf16=True)
+    h = tobf_bits(rng.standard_normal((T, d)) * 3.0)
+    hd = np_widen(h)
+    u = tobf_bits(hd / np.sqrt(np.mean(hd * hd, axis=1, keepdims=True) + eps))
+    ud, W1d, W3d, W2d = (np_widen(a) for a in (u, W1, W3, W2))
+    l = ud @ Wg.astype(np.float64).T
+    kth = np.sort(l, axis=1)[:, -K][:, None]
+    masked = np.where(l >= kth, l, -np.inf)
+    G = np.exp(masked - masked.max(1, keepdims=True))
+    G /= G.sum(1, keepdims=True)
+    y = sum(G[:, [e]] * np_expert(ud, W1d, W3d, W2d, e) for e in range(n))
+    ref = oracle.block_forward(h, Wg, W1, W3, W2, K, eps)
+    assert np.array_equal(ref["u"], u)
+    assert np.max(np.abs(ref["h_new"] - (hd + y))) <= 1e-12 * np.abs(hd + y).max()
+    assert np.array_equal(ref["h_bits"], oracle.round_bf16(hd + y))
+
+
+def test_block_with_zero_W2_is_identity():
+    rng = np.random.default_rng(13)
+    _, Wg, W1, W3, W2 = rand_layer(rng, 5, 8, 12, 8, bf16=True)
+    h = tobf_bits(rng.standard_normal((5, 8)))
+    ref = oracle.block_forward(h, Wg, W1, W3, np.zeros_like(W2), 2, 1e-5)
+    assert np.array_equal(ref["h_bits"], h)
+    assert np.all(ref["y"] == 0.0)

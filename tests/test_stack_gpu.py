@@ -1,0 +1,276 @@
+"""Residual blocks and the layer stack (h <- h + MoE(RMSNorm(h)), per layer) on the
+GPU through the C ABI, against the fp64 oracle's own trajectory.
+
+The oracle starts from the same seeded h0 and follows its own fp64 path, storing
+h and the MoE input u in bf16 where the model does; no value from the GPU enters
+it.  Tolerance at layer l, elementwise, beyond the storage rounding of h_l itself:
+
+    |h_gpu - h_ref| - 2^-8 |h_ref|  <=  G * sum_{j<=l} ( 1e-2 rms(y_j) + [j<l] 2^-8 |h_ref,j| )
+
+i.e. the single-layer arithmetic bound (1e-2 rms of the MoE output, as for one
+layer) plus the earlier layers' storage roundings of h, summed over the layers
+so far, with G = 2 for the growth of earlier differences through later layers
+(the residual path passes them on unchanged; the MoE path sees them through
+RMSNorm, with a gain of about rms(y)/rms(h) < 1 here).
+
+Near ties.  The GPU's rows differ from the oracle's by a few bf16 ulps at the
+first layer and drift further apart with depth, so a token whose oracle logits
+sit close to a selection boundary may take another expert on the GPU -- both
+choices are right to within the precision.  A token is excluded from the
+elementwise check from the first layer at which the gap between its oracle
+logits of ranks K and K+1 (or 1..K) is below
+
+    TIE(t) = max(tie_min, 4 * ||u_gpu(t) - u_ref(t)||_2 * sigma(W_g)),
+
+the logit shift that 4 standard deviations of the router's random weights can
+make of the token's normalised-state deviation carried into the layer (its
+measured deviation at the previous layer over rms(h)).  Excluded tokens are
+counted and must stay finite.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import BF16_STORE, BF16_TOL, near_tie_mask
+from sparse_mixture_experts_54_b300 import _lib, inputs
+from sparse_mixture_experts_54_b300.layer import MoELayer
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-5
+GROWTH = 2.0
+
+
+def make_h(T, d, seed, scale=3.0, dtype=torch.bfloat16):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return (torch.randn((T, d), generator=g, device="cuda") * scale).to(dtype).contiguous()
+
+
+def layer_weights(w, seed):
+    Wg, _ = inputs.make_router(w, "cuda", seed=seed)
+    W1, W3, W2 = inputs.make_experts(w, "cuda", seed=seed)
+    return Wg, W1, W3, W2
+
+
+class Trajectory:
+    """Oracle trajectory of a set of token rows through successive blocks, with the
+    accumulated tolerance and the near-tie exclusion of each row.  bf16 rows use
+    the bf16 bound (1e-2 rms(y) per layer, half an ulp = 2^-8 |h| of storage);
+    fp32 rows the fp32 one (1e-5 max|y| per layer, 2^-24 |h|)."""
+
+    def __init__(self, h0, K, tie):
+        self.h = h0
+        self.K = K
+        self.tie = tie
+        self.f32 = h0.dtype == np.float32
+        self.store = 2.0 ** -24 if self.f32 else BF16_STORE
+        self.budget = np.zeros(h0.shape, dtype=np.float64)   # sum of the per-layer terms so far
+        self.excluded = np.zeros(h0.shape[0], dtype=bool)
+        self.dev_u = np.zeros(h0.shape[0], dtype=np.float64)  # ||u_gpu - u_ref||_2 carried into the next layer
+
+    def step(self, Wg, W1, W3, W2, bias=None):
+        ref = oracle.block_forward(self.h, Wg, W1, W3, W2, self.K, EPS, bias)
+        sigma_g = float(np.sqrt(np.mean(np.asarray(Wg, dtype=np.float64) ** 2)))
+        tie = np.maximum(self.tie, 4.0 * self.dev_u * sigma_g)
+        s_l = -np.sort(-ref["logits"], axis=1)
+        m = min(self.K + 1, s_l.shape[1])
+        gaps = (s_l[:, : m - 1] - s_l[:, 1:m]).min(axis=1)
+        self.excluded |= gaps < tie
+        if self.f32:
+            arith = 1e-5 * np.max(np.abs(ref["y"]))
+        else:
+            arith = BF16_TOL * np.sqrt(np.mean(ref["y"] ** 2, axis=1, keepdims=True))
+        self.budget = self.budget + arith
+        allowed = self.store * np.abs(ref["h_new"]) + GROWTH * self.budget
+        # this layer's storage rounding becomes part of the next layers' budget
+        self.budget = self.budget + self.store * np.abs(ref["h_new"])
+        self.h = ref["h_bits"]
+        return ref, allowed
+
+    def check(self, h_gpu_rows, ref, allowed, what):
+        hg = h_gpu_rows.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(hg)), f"{what}: non-finite output"
+        keep = ~self.excluded
+        diff = np.abs(hg - ref["h_new"])
+        rms_h = np.sqrt(np.mean(ref["h_new"] ** 2, axis=1))
+        new_dev = np.sqrt(np.sum(diff ** 2, axis=1)) / rms_h
+        excess = (diff - allowed)[keep]
+        worst = float(excess.max()) if excess.size else -1.0
+        if worst > 0.0:
+            rows = np.nonzero(keep)[0]
+            bad = rows[np.argmax((diff - allowed)[keep].max(axis=1))]
+            s_l = -np.sort(-ref["logits"][bad])
+            raise AssertionError(
+                f"{what}: error exceeds the bound by {worst:.3e} (raw max {diff[keep].max():.3e}); row {bad}: "
+                f"oracle logits {np.round(s_l[:4], 4).tolist()}, deviation carried in "
+                f"{self.dev_u[bad]:.3e}, now {new_dev[bad]:.3e}")
+        self.dev_u = new_dev
+        return float(np.max(diff[keep])) if keep.any() else 0.0
+
+
+def run_block_case(T, d, F, n, K, path=0, pair=0, dtype=torch.bfloat16, seed=0):
+    w = inputs.Workload("blk", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=seed,
+                        dtype="f32" if dtype == torch.float32 else "bf16")
+    m = MoELayer(d, F, n, K, dtype=dtype)
+    if path:
+        m.set_option(_lib.MOE_OPT_FORCE_PATH, path)
+    if pair:
+        m.set_option(_lib.MOE_OPT_GEMM_PAIR, pair)
+    Wg, W1, W3, W2 = layer_weights(w, seed)
+    h = make_h(T, d, seed + 7, dtype=dtype)
+    tr = Trajectory(inputs.to_oracle(h), K, tie=1e-3)
+    host = tuple(inputs.to_oracle(t) for t in (Wg, W1, W3, W2))
+    m.block_forward(h, Wg, W1, W3, W2, EPS)
+    torch.cuda.synchronize()
+    assert m.status() == 0, _lib.moe_error_string(m.status())
+    ref, allowed = tr.step(*host)
+    err = tr.check(h, ref, allowed, f"block T={T} d={d} F={F} n={n} K={K} path={path} pair={pair}")
+    return err, int(tr.excluded.sum())
+
+
+@pytest.mark.parametrize("T,path,pair", [(300, 1, 1), (300, 1, 2), (300, 0, 0), (40, 2, 0), (1, 0, 0)])
+def test_block_matches_oracle_bf16(T, path, pair):
+    err, excl = run_block_case(T, 256, 384, 8, 2, path=path, pair=pair, seed=T + path)
+    print(f"block T={T}: max err {err:.3e}, near-tie tokens {excl}")
+
+
+def test_block_matches_oracle_fp32():
+    err, excl = run_block_case(64, 128, 256, 8, 2, dtype=torch.float32, seed=5)
+    print(f"block fp32: max err {err:.3e}, near-tie tokens {excl}")
+
+
+def test_block_rejects_negative_eps():
+    m = MoELayer(256, 256, 8, 2)
+    h = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
+    Wg = torch.zeros((8, 256), dtype=torch.float32, device="cuda")
+    W = torch.zeros((8, 256, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(_lib.MoEError) as ei:
+        m.block_forward(h, Wg, W, W, W, eps=-1.0)
+    assert ei.value.code == _lib.MOE_ERR_INVALID
+
+
+def test_small_stack_layer_by_layer_and_in_one_call():
+    # 4 layers, both GEMM paths in use (T above the decode threshold)
+    L, T, d, F, n, K = 4, 200, 256, 256, 8, 2
+    w = inputs.Workload("stk", T=T, d=d, d_ff=F, n_experts=n, k=K)
+    layers = [layer_weights(w, 1000 + l) for l in range(L)]
+    m = MoELayer(d, F, n, K)
+    h0 = make_h(T, d, 31)
+    h = h0.clone()
+    tr = Trajectory(inputs.to_oracle(h0), K, tie=1e-3)
+    errs = []
+    for l, lw in enumerate(layers):
+        m.block_forward(h, *lw, EPS)
+        torch.cuda.synchronize()
+        ref, allowed = tr.step(*(inputs.to_oracle(t) for t in lw))
+        errs.append(tr.check(h, ref, allowed, f"layer {l}"))
+    assert m.status() == 0
+    h2 = h0.clone()
+    m.stack_forward(h2, layers, EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h2), "one stack call differs from the same blocks called one by one"
+    print(f"stack of {L}: max err per layer {['%.2e' % e for e in errs]}, near-tie tokens {int(tr.excluded.sum())}")
+
+
+def test_stack_zero_experts_keeps_h():
+    # W2 = 0 in every layer: MoE(...) = 0, so h passes through unchanged (bitwise)
+    L, T, d, F = 3, 100, 256, 128
+    w = inputs.Workload("stk0", T=T, d=d, d_ff=F)
+    layers = []
+    for l in range(L):
+        Wg, W1, W3, W2 = layer_weights(w, 50 + l)
+        layers.append((Wg, W1, W3, torch.zeros_like(W2)))
+    m = MoELayer(d, F, 8, 2)
+    h0 = make_h(T, d, 3)
+    h = h0.clone()
+    m.stack_forward(h, layers, EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h0)
+
+
+# ----------------------------------------------------------------------------- Mixtral-shape 32-layer stack
+@pytest.fixture(scope="module")
+def mixtral_stack():
+    """The 32 layers of the stack workload (layer l seeded 1000 + l): ~90 GB of
+    expert weights resident on the device."""
+    w = inputs.workload("decode_t32")
+    layers = [layer_weights(w, 1000 + l) for l in range(inputs.STACK_LAYERS)]
+    yield w, layers
+    del layers
+    torch.cuda.empty_cache()
+
+
+def bits_to_device(bits):
+    """Oracle-held bf16 bit patterns as a device tensor (oracle -> GPU only)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+@pytest.mark.slow
+def test_mixtral_stack32_every_layer_from_the_oracle_state(mixtral_stack):
+    """Each of the 32 layers at the Mixtral shape, started from the oracle's own
+    state: the oracle carries 8 decode rows and 4 sampled rows of a T=8192 prefill
+    batch through the stack in fp64/bf16; before each layer those rows are copied
+    into the GPU's batches (the prefill batch's other rows follow the GPU's own
+    path -- rows do not interact), the GPU runs the block, and its rows must match
+    the oracle's next state within the single-layer bound.  Two independent bf16
+    trajectories drift apart by ~1% of rms(h) within ten layers, so near ties
+    make a whole-stack comparison of the two paths meaningless at this depth."""
+    w, layers = mixtral_stack
+    T_dec, T_pre, n_pre = 8, inputs.STACK_PREFILL_T, 4
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    m.reserve(T_pre)
+    hp = inputs.make_x(w, "cuda", seed=2001, T=T_pre)
+    toks = inputs.sample_tokens(T_pre, n_pre, seed=3).numpy()
+    toks_d = torch.from_numpy(toks).cuda()
+    rows = np.concatenate([inputs.to_oracle(inputs.make_x(w, "cuda", seed=2000, T=T_dec)),
+                           inputs.to_oracle(hp)[toks]], axis=0)
+    errs, near_total = [], 0
+    for l, lw in enumerate(layers):
+        ref = oracle.block_forward(rows, *(inputs.to_oracle(t) for t in lw), w.k, EPS)
+        hd = bits_to_device(rows[:T_dec])
+        hp[toks_d] = bits_to_device(rows[T_dec:])
+        m.block_forward(hd, *lw, EPS)
+        m.block_forward(hp, *lw, EPS)
+        torch.cuda.synchronize()
+        assert m.status() == 0, f"layer {l}: {_lib.moe_error_string(m.status())}"
+        got = torch.cat([hd, hp[toks_d]], dim=0).float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got))
+        near = near_tie_mask(ref["logits"], w.k, 1e-3)
+        near_total += int(near.sum())
+        y_rms = np.sqrt(np.mean(ref["y"] ** 2, axis=1, keepdims=True))
+        allowed = BF16_STORE * np.abs(ref["h_new"]) + BF16_TOL * y_rms
+        diff = np.abs(got - ref["h_new"])
+        excess = (diff - allowed)[~near]
+        assert excess.size == 0 or excess.max() <= 0.0, \
+            f"layer {l}: error beyond the bound by {excess.max():.3e} (raw max {diff[~near].max():.3e})"
+        errs.append(float((diff - BF16_STORE * np.abs(ref["h_new"]))[~near].max() / y_rms.max()))
+        rows = ref["h_bits"]
+    print(f"stack32 from the oracle state: max error beyond storage rounding, per layer, in units of "
+          f"rms(y): max {max(errs):.2e}, mean {np.mean(errs):.2e}; near-tie rows {near_total} of {12 * len(layers)}")
+
+
+@pytest.mark.slow
+def test_mixtral_stack32_one_call_equals_block_by_block(mixtral_stack):
+    # the GPU's own trajectory: one moe_stack_forward call over the 32 layers is the
+    # same computation as 32 moe_block_forward calls, bit for bit, on the decode path
+    # (T=8) and the grouped path (T=8192); the result stays finite with rms growing
+    # no more than the residual sum of 32 layer outputs allows
+    w, layers = mixtral_stack
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    m.reserve(inputs.STACK_PREFILL_T)
+    for T, seed in ((8, 2100), (inputs.STACK_PREFILL_T, 2101)):
+        h0 = inputs.make_x(w, "cuda", seed=seed, T=T)
+        a, b = h0.clone(), h0.clone()
+        for lw in layers:
+            m.block_forward(a, *lw, EPS)
+        m.stack_forward(b, layers, EPS)
+        torch.cuda.synchronize()
+        assert m.status() == 0
+        assert torch.equal(a, b)
+        af = a.float()
+        assert torch.isfinite(af).all()
+        rms = float(af.pow(2).mean().sqrt())
+        assert 1.0 < rms < 32.0, rms
+        print(f"stack32 T={T}: rms(h) 1.0 -> {rms:.3f} after 32 layers")
