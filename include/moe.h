@@ -69,12 +69,10 @@ typedef enum {
     MOE_OPT_WAIT_LIMIT_US = 2, /* wall-time limit of every bounded wait inside a kernel (default 2,000,000 us) */
     MOE_OPT_FORCE_PATH = 3,    /* 0 = choose by T, 1 = always grouped GEMM, 2 = always decode kernels */
     MOE_OPT_STAGE_TIMING = 4,  /* 1 = record CUDA events around every kernel of moe_forward (see moe_stage_times) */
-    MOE_OPT_GEMM_PAIR = 5,     /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
+    MOE_OPT_GEMM_PAIR = 5      /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
                                   CTA pairs -- tcgen05 cta_group::2, 256/128-row tiles -- when the device can
                                   co-schedule them), 1 = both single-CTA, 2 = both on CTA pairs or
                                   MOE_ERR_UNSUPPORTED */
-    MOE_OPT_L2_PREFETCH = 6    /* grouped GEMMs: prefetch operand tiles into L2 this many 64-wide k-steps ahead of
-                                  their loads (0 = off, the default); process-wide, not per context */
 } moe_option_t;
 
 /*

@@ -31,7 +31,6 @@ MOE_OPT_WAIT_LIMIT_US = 2
 MOE_OPT_FORCE_PATH = 3
 MOE_OPT_STAGE_TIMING = 4
 MOE_OPT_GEMM_PAIR = 5
-MOE_OPT_L2_PREFETCH = 6
 
 # Every entry point declared in include/moe.h, with its ctypes signature.
 _P = ctypes.c_void_p

@@ -124,14 +124,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
         : "memory");
 }
 
-// Ask for a 2-D tile to be brought into L2 (no shared memory, no completion
-// signal): issued some k-steps ahead of the real load so that it hits L2.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, loads
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

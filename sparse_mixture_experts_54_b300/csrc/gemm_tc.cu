@@ -57,7 +57,6 @@ struct TcArgs {
     int kblocks;          // K / BK
     int ntiles;           // N-tiles per expert
     int group_m;          // row blocks per tile group (see tc_decode_tile)
-    int pf_dist;          // k-steps ahead at which the producer prefetches operand tiles into L2 (0: off)
     int b_rows_per_e;     // rows of the B tensor per expert (F for MODE 0, d for MODE 1)
     __nv_bfloat16* H;     // MODE 0 output, [R][F]
     int ldH;
@@ -160,39 +159,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            // L2 prefetch: the operand tiles pf_dist k-steps ahead of the loads,
-            // running on into this CTA's next tile
-            auto tile_rows = [&](int t, int& ar, int& br) {
-                int e2, mb2, nb2;
-                tc_decode_tile(prefix, n, p.ntiles, p.group_m, t, e2, mb2, nb2);
-                ar = offsets[e2] + mb2 * BM;
-                br = e2 * p.b_rows_per_e + nb2 * (MODE == 0 ? 128 : 256);
-            };
-            auto prefetch = [&](int ar, int br, int kb) {
-                tma_prefetch_l2_2d(&tmA, kb * BK, ar);
-                tma_prefetch_l2_2d(&tmB0, kb * BK, br);
-                if (MODE == 0) tma_prefetch_l2_2d(&tmB1, kb * BK, br);
-            };
-            const int pf = p.pf_dist < p.kblocks ? p.pf_dist : p.kblocks;
-            if (pf > 0 && static_cast<int>(blockIdx.x) < total) {
-                int ar, br;
-                tile_rows(blockIdx.x, ar, br);
-                for (int kb = 0; kb < pf; ++kb) prefetch(ar, br, kb);
-            }
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 int e, mb, nb;
                 tc_decode_tile(prefix, n, p.ntiles, p.group_m, tile, e, mb, nb);
                 const int arow = offsets[e] + mb * BM;
                 const int brow = e * p.b_rows_per_e + nb * (MODE == 0 ? 128 : 256);
-                int next_ar = 0, next_br = 0;
-                const bool has_next = tile + static_cast<int>(gridDim.x) < total;
-                if (pf > 0 && has_next) tile_rows(tile + gridDim.x, next_ar, next_br);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (pf > 0) {
-                        const int kp = kb + pf;
-                        if (kp < p.kblocks) prefetch(arow, brow, kp);
-                        else if (has_next) prefetch(next_ar, next_br, kp - p.kblocks);
-                    }
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
                     const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
                     const uint32_t b_dst = a_dst + A_BYTES;
@@ -346,10 +318,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------------------
 // host side
-static int g_l2_prefetch = 0;
-int gemm_l2_prefetch_distance() { return g_l2_prefetch; }
-void set_gemm_l2_prefetch_distance(int k_steps) { g_l2_prefetch = k_steps < 0 ? 0 : k_steps; }
-
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -381,7 +349,6 @@ bool encode_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint6
 template <int MODE>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, TcArgs args,
                              int num_sms, cudaStream_t s) {
-    args.pf_dist = gemm_l2_prefetch_distance();
     // Weights are read by every 128-row block of their expert at about the same
     // time; keeping them at high L2 priority measured ~3% fewer cycles than
     // evict_first on the T=4096 prefill.

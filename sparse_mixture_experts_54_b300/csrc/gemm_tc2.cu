@@ -71,7 +71,6 @@ struct PairArgs {
     int kblocks;          // K / 64
     int ntiles;           // N blocks per expert
     int group_m;          // 256-row blocks per tile group
-    int pf_dist;          // k-steps ahead at which the producer prefetches operand tiles into L2 (0: off)
     int b_rows_per_e;     // rows of the B tensors per expert (F for MODE 0, d for MODE 1)
     __nv_bfloat16* H;     // MODE 0 output [R][F]
     int ldH;
@@ -200,37 +199,11 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
                      (MODE == 0 ? nb2 * 128 + (hf ? 64 * static_cast<int>(rank) : 0)
                                 : nb2 * 256 + static_cast<int>(rank) * 128);
             };
-            // L2 prefetch of the tiles pf_dist k-steps ahead (whole 128-row boxes)
-            auto prefetch = [&](int ar, int br, bool hf, int kb) {
-                tma_prefetch_l2_2d(&tmA, kb * Q_BK, ar);
-                if (MODE == 0 && hf) {
-                    tma_prefetch_l2_2d(&tmB0h, kb * Q_BK, br);
-                    tma_prefetch_l2_2d(&tmB1h, kb * Q_BK, br);
-                } else {
-                    tma_prefetch_l2_2d(mapB, kb * Q_BK, br);
-                }
-            };
-            const int pf = p.pf_dist < p.kblocks ? p.pf_dist : p.kblocks;
-            if (pf > 0 && cid < total) {
-                int ar, br;
-                bool hf;
-                tile_rows(cid, ar, br, hf);
-                for (int kb = 0; kb < pf; ++kb) prefetch(ar, br, hf, kb);
-            }
             for (int tile = cid; tile < total && ok; tile += ncl) {
                 int arow, brow;
                 bool half;
                 tile_rows(tile, arow, brow, half);
-                int next_ar = 0, next_br = 0;
-                bool next_half = false;
-                const bool has_next = tile + ncl < total;
-                if (pf > 0 && has_next) tile_rows(tile + ncl, next_ar, next_br, next_half);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (pf > 0) {
-                        const int kp = kb + pf;
-                        if (kp < p.kblocks) prefetch(arow, brow, half, kp);
-                        else if (has_next) prefetch(next_ar, next_br, next_half, kp - p.kblocks);
-                    }
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
                     const uint32_t a_dst = tiles_u32 + stage * Q_STAGE_BYTES;
                     const uint32_t b_dst = a_dst + Q_A_BYTES;
@@ -452,7 +425,6 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
                         const CUtensorMap& b1h, PairArgs args, int num_sms, cudaStream_t s) {
     const int nc = pair_clusters<MODE>(num_sms);
     if (nc <= 0) return cudaErrorNotSupported;
-    args.pf_dist = gemm_l2_prefetch_distance();
     auto kern = tc_pair_gemm_kernel<MODE>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * nc);

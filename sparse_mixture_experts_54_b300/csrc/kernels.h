@@ -29,11 +29,6 @@ inline int tile_group_rows(int rows_per_block, int k_elems) {
     return g < 1 ? 1 : static_cast<int>(g);
 }
 
-// k-steps ahead at which the grouped GEMMs' producers prefetch operand tiles
-// into L2 (0 = off); process-wide, set through MOE_OPT_L2_PREFETCH.
-int gemm_l2_prefetch_distance();
-void set_gemm_l2_prefetch_distance(int k_steps);
-
 // Launch with programmatic stream serialisation (see griddep_wait).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,

@@ -393,10 +393,6 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
             c->force_path = static_cast<int>(value);
             return MOE_OK;
-        case MOE_OPT_L2_PREFETCH:
-            if (value < 0 || value > 1024) return MOE_ERR_INVALID;
-            set_gemm_l2_prefetch_distance(static_cast<int>(value));
-            return MOE_OK;
         case MOE_OPT_GEMM_PAIR:
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
             c->gemm_pair = static_cast<int>(value);
