@@ -69,10 +69,12 @@ typedef enum {
     MOE_OPT_WAIT_LIMIT_US = 2, /* wall-time limit of every bounded wait inside a kernel (default 2,000,000 us) */
     MOE_OPT_FORCE_PATH = 3,    /* 0 = choose by T, 1 = always grouped GEMM, 2 = always decode kernels */
     MOE_OPT_STAGE_TIMING = 4,  /* 1 = record CUDA events around every kernel of moe_forward (see moe_stage_times) */
-    MOE_OPT_GEMM_PAIR = 5      /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
+    MOE_OPT_GEMM_PAIR = 5,     /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
                                   CTA pairs -- tcgen05 cta_group::2, 256/128-row tiles -- when the device can
                                   co-schedule them), 1 = both single-CTA, 2 = both on CTA pairs or
                                   MOE_ERR_UNSUPPORTED */
+    MOE_OPT_HOST_OUTPUT = 6    /* moe_forward_host: 0 = copy y back on the stream (default), 1 = when y_host is
+                                  pinned, the layer's last kernel writes y into it directly over the bus */
 } moe_option_t;
 
 /*
@@ -147,9 +149,13 @@ int moe_forward(moe_ctx* ctx, const void* x, const float* W_g, const void* W1, c
 /*
  * moe_forward with x and y in host memory (pinned memory gives asynchronous
  * copies; pageable memory works but the copies then synchronise).  Copies x
- * to a context-owned device buffer, runs the layer and copies y back, all on
- * `stream`.  Weights stay device pointers.  The host buffers must stay valid
- * until the stream reaches this point.
+ * to one of two context-owned device buffers on a stream of the context's own
+ * (so that, with pinned memory, the copy overlaps the previous call's
+ * kernels), runs the layer on `stream` once the copy is done, and copies y
+ * back on `stream`.  Weights stay device pointers.  When `stream` reaches this
+ * point, y_host holds the result; x_host must stay valid and unchanged until
+ * then.  While `stream` is being captured into a graph, all of it runs on
+ * `stream`.
  */
 int moe_forward_host(moe_ctx* ctx, const void* x_host, const float* W_g, const void* W1,
                      const void* W3, const void* W2, void* y_host, int T, moe_stream_t stream);

@@ -31,6 +31,7 @@ MOE_OPT_WAIT_LIMIT_US = 2
 MOE_OPT_FORCE_PATH = 3
 MOE_OPT_STAGE_TIMING = 4
 MOE_OPT_GEMM_PAIR = 5
+MOE_OPT_HOST_OUTPUT = 6
 
 # Every entry point declared in include/moe.h, with its ctypes signature.
 _P = ctypes.c_void_p

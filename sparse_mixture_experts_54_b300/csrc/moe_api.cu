@@ -19,6 +19,7 @@ struct moe_ctx {
     long long wait_limit_us = 2000000;
     int force_path = 0;
     int gemm_pair = 0;          // 0 auto, 1 single CTA, 2 CTA pairs
+    int host_out = 0;           // moe_forward_host: 1 = kernels write y into pinned host memory directly
     int device = 0;
     int num_sms = 148;
     int* status_host = nullptr;   // host-mapped
@@ -40,7 +41,13 @@ struct moe_ctx {
     void* H = nullptr;
     float* Ys = nullptr;
     void* xbuf = nullptr;
+    void* xbuf2 = nullptr;      // moe_forward_host stages x in xbuf / xbuf2 on alternate calls
     void* ybuf = nullptr;
+    // moe_forward_host: input copies on a stream of their own, overlapping the previous call
+    cudaStream_t h2d_stream = nullptr;
+    cudaEvent_t ev_h2d[2] = {nullptr, nullptr};
+    cudaEvent_t ev_xfree[2] = {nullptr, nullptr};
+    int host_slot = 0;
     float* Pa = nullptr;        // decode partial sums [S][R][F] (W1 rows), [S][R][F] (W3 rows)
     float* Pb = nullptr;
     float* P2 = nullptr;        // decode partial sums [S][R][d] (W2 rows)
@@ -58,7 +65,7 @@ size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, rstd, Xp, H, Ys, xbuf, ybuf, Pa, Pb, P2, total;
+    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, rstd, Xp, H, Ys, xbuf, xbuf2, ybuf, Pa, Pb, P2, total;
 };
 
 Layout layout_for(const moe_ctx* c, int T, int Tdec) {
@@ -80,6 +87,7 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.H = take(R * c->F * es);
     L.Ys = take(R * c->d * 4);
     L.xbuf = take(Tn * c->d * es);
+    L.xbuf2 = take(Tn * c->d * es);
     L.ybuf = take(Tn * c->d * es);
     const size_t Rd = static_cast<size_t>(c->k) * static_cast<size_t>(Tdec > 0 ? Tdec : 0);
     L.Pa = take(kDecodeMaxSplits * Rd * c->F * 4);
@@ -148,6 +156,7 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->H = b + L.H;
     c->Ys = reinterpret_cast<float*>(b + L.Ys);
     c->xbuf = b + L.xbuf;
+    c->xbuf2 = b + L.xbuf2;
     c->ybuf = b + L.ybuf;
     c->Pa = reinterpret_cast<float*>(b + L.Pa);
     c->Pb = reinterpret_cast<float*>(b + L.Pb);
@@ -169,6 +178,34 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
 }
 
 bool tc_shape_ok(const moe_ctx* c) { return c->d % 256 == 0 && c->F % 128 == 0; }
+
+// Device address of pinned, mapped host memory (pinned allocations are mapped
+// on every 64-bit system with unified addressing), or null for anything else.
+void* mapped_host_alias(void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+    return a.devicePointer;
+}
+
+// The input-copy stream and its events (created on first use).
+bool ensure_copy_stream(moe_ctx* c) {
+    if (c->h2d_stream) return true;
+    cudaStream_t st = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return false;
+    for (int i = 0; i < 2; ++i) {
+        if (cudaEventCreateWithFlags(&c->ev_h2d[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&c->ev_xfree[i], cudaEventDisableTiming) != cudaSuccess) {
+            cudaStreamDestroy(st);
+            return false;
+        }
+    }
+    c->h2d_stream = st;
+    return true;
+}
 
 // The weight-streaming kernels serve bf16 batches of up to decode_max_t tokens.
 bool use_decode(const moe_ctx* c, int T) {
@@ -393,6 +430,10 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
             c->force_path = static_cast<int>(value);
             return MOE_OK;
+        case MOE_OPT_HOST_OUTPUT:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID;
+            c->host_out = static_cast<int>(value);
+            return MOE_OK;
         case MOE_OPT_GEMM_PAIR:
             if (value < 0 || value > 2) return MOE_ERR_INVALID;
             c->gemm_pair = static_cast<int>(value);
@@ -512,9 +553,32 @@ int moe_forward_host(moe_ctx* c, const void* x_host, const float* Wg, const void
     int rc = ensure_workspace(c, T, s, use_decode(c, T));
     if (rc != MOE_OK) return rc;
     const size_t bytes = static_cast<size_t>(T) * c->d * esize(c->dtype);
-    if (cudaMemcpyAsync(c->xbuf, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-    rc = run_forward(c, c->xbuf, Wg, W1, W3, W2, c->ybuf, T, s);
-    if (rc != MOE_OK) return rc;
+    // The input copy runs on the context's own stream into one of two staging
+    // buffers, so it can overlap the previous call's kernels; the layer and the
+    // output copy stay on `stream`.  Reusing a staging buffer waits for the call
+    // that read it.  While `stream` is being captured, everything stays on it.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const bool capturing = cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+    void* xb = c->xbuf;
+    if (!capturing && ensure_copy_stream(c)) {
+        const int b = c->host_slot;
+        c->host_slot ^= 1;
+        xb = b ? c->xbuf2 : c->xbuf;
+        if (cudaStreamWaitEvent(c->h2d_stream, c->ev_xfree[b], 0) != cudaSuccess ||
+            cudaMemcpyAsync(xb, x_host, bytes, cudaMemcpyHostToDevice, c->h2d_stream) != cudaSuccess ||
+            cudaEventRecord(c->ev_h2d[b], c->h2d_stream) != cudaSuccess || cudaStreamWaitEvent(s, c->ev_h2d[b], 0) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        void* y_direct = c->host_out ? mapped_host_alias(y_host) : nullptr;
+        rc = run_forward(c, xb, Wg, W1, W3, W2, y_direct ? y_direct : c->ybuf, T, s);
+        if (rc != MOE_OK) return rc;
+        if (cudaEventRecord(c->ev_xfree[b], s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (y_direct) return MOE_OK;   // the kernels wrote y into host memory
+    } else {
+        cudaGetLastError();
+        if (cudaMemcpyAsync(xb, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+        rc = run_forward(c, xb, Wg, W1, W3, W2, c->ybuf, T, s);
+        if (rc != MOE_OK) return rc;
+    }
     if (cudaMemcpyAsync(y_host, c->ybuf, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }
@@ -598,6 +662,14 @@ void moe_destroy(moe_ctx* c) {
     if (!c) return;
     for (auto& ev : c->ev_calls) c->ev_free.insert(c->ev_free.end(), ev.begin(), ev.begin() + kStages + 1);
     for (cudaEvent_t e : c->ev_free) cudaEventDestroy(e);
+    if (c->h2d_stream) {
+        cudaStreamSynchronize(c->h2d_stream);
+        cudaStreamDestroy(c->h2d_stream);
+    }
+    for (int i = 0; i < 2; ++i) {
+        if (c->ev_h2d[i]) cudaEventDestroy(c->ev_h2d[i]);
+        if (c->ev_xfree[i]) cudaEventDestroy(c->ev_xfree[i]);
+    }
     if (c->ws) cudaFree(c->ws);
     if (c->status_host) cudaFreeHost(c->status_host);
     delete c;

@@ -54,8 +54,7 @@ namespace moe {
 namespace {
 constexpr int FR_THREADS = 512;
 constexpr int FR_WARPS = 16;
-constexpr int FR_DS = 4;                    // warps that split one row
-constexpr int FR_TG = FR_WARPS / FR_DS;     // token groups per block
+constexpr int FR_DS_LARGE = 4;              // warps that split one row (batches of many tokens)
 constexpr int FR_ROUND = FR_THREADS;        // assignments placed per round in phase 2
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
@@ -188,10 +187,15 @@ __device__ __forceinline__ int fr_index(int lane, int i) {
     return idx;
 }
 
-template <typename TX, int NMAX, int TOKW, bool NORM>
+// SMALL (one token per block, small batches): all 16 warps split the row and
+// W_g is read from L2 instead of being staged in shared memory first, which
+// would cost more latency than the one token's dot products.
+template <typename TX, int NMAX, int TOKW, bool NORM, bool SMALL>
 __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteArgs p) {
+    constexpr int FR_DS = SMALL ? FR_WARPS : FR_DS_LARGE;   // warps that split one row
+    constexpr int FR_TG = FR_WARPS / FR_DS;                 // token groups per block
     extern __shared__ __align__(16) unsigned char fr_smem[];
-    float* wg_s = reinterpret_cast<float*>(fr_smem);
+    const float* wg_s = SMALL ? p.Wg : reinterpret_cast<const float*>(fr_smem);
     float* red = reinterpret_cast<float*>(fr_smem + p.red_off);   // [FR_DS][TPB][NMAX]
     __shared__ int s_hist[32], s_cnt[32], s_pre[32], s_base[32], s_run[32];
     __shared__ int wtab[FR_WARPS][33];
@@ -206,10 +210,10 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
 
     // W_g is written by no kernel of the layer: stage it before waiting on the
     // previous kernel.
-    {
+    if (!SMALL) {
         const int total4 = n * d / 4;
         const float4* src = reinterpret_cast<const float4*>(p.Wg);
-        float4* dst = reinterpret_cast<float4*>(wg_s);
+        float4* dst = reinterpret_cast<float4*>(fr_smem);
         for (int i0 = tid; i0 < total4; i0 += 8 * FR_THREADS) {
             float4 v[8];
 #pragma unroll
@@ -317,8 +321,14 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
             for (int e = 0; e < NMAX; ++e) {
                 if (e < n) {
                     const float* w = wg_s + static_cast<size_t>(e) * d;
-                    const float4 w0 = h0 ? *reinterpret_cast<const float4*>(w + j0) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 w1 = h1 ? *reinterpret_cast<const float4*>(w + j1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;
+                    if (SMALL) {
+                        if (h0) w0 = __ldg(reinterpret_cast<const float4*>(w + j0));
+                        if (h1) w1 = __ldg(reinterpret_cast<const float4*>(w + j1));
+                    } else {
+                        if (h0) w0 = *reinterpret_cast<const float4*>(w + j0);
+                        if (h1) w1 = *reinterpret_cast<const float4*>(w + j1);
+                    }
                     const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int j = 0; j < TOKW; ++j) {
@@ -524,19 +534,26 @@ int fused_route_blocks(int T, int num_sms) {
     return (T + chunk - 1) / chunk;
 }
 
-template <typename TX, int NMAX, int TOKW, bool NORM>
-static cudaError_t launch_fused_n(FusedRouteArgs& a, int G, cudaStream_t s) {
-    constexpr int TPB = FR_TG * TOKW;
-    const size_t wg_bytes = static_cast<size_t>(a.n) * a.d * 4;
+template <typename TX, int NMAX, int TOKW, bool NORM, bool SMALL>
+static cudaError_t launch_fused_s(FusedRouteArgs& a, int G, cudaStream_t s) {
+    constexpr int DS = SMALL ? FR_WARPS : FR_DS_LARGE;
+    constexpr int TPB = (FR_WARPS / DS) * TOKW;
+    const size_t wg_bytes = SMALL ? 0 : static_cast<size_t>(a.n) * a.d * 4;
     const size_t p2_bytes = FR_ROUND * sizeof(int2);
     size_t base = wg_bytes > p2_bytes ? wg_bytes : p2_bytes;
     base = (base + 15) & ~static_cast<size_t>(15);
     a.red_off = base;
-    const size_t smem = base + static_cast<size_t>(FR_DS) * TPB * NMAX * 4;
-    auto kern = route_fused_kernel<TX, NMAX, TOKW, NORM>;
+    const size_t smem = base + static_cast<size_t>(DS) * TPB * NMAX * 4;
+    auto kern = route_fused_kernel<TX, NMAX, TOKW, NORM, SMALL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(G), dim3(FR_THREADS), smem, s, a);
+}
+
+template <typename TX, int NMAX, int TOKW, bool NORM>
+static cudaError_t launch_fused_n(FusedRouteArgs& a, int G, cudaStream_t s) {
+    if (a.chunk == 1) return launch_fused_s<TX, NMAX, 1, NORM, true>(a, G, s);
+    return launch_fused_s<TX, NMAX, TOKW, NORM, false>(a, G, s);
 }
 
 template <typename TX, int NMAX, int TOKW>

@@ -144,6 +144,27 @@ def test_forward_is_bitwise_deterministic_and_host_entry_matches():
     assert m.status() == 0
 
 
+def test_host_entry_back_to_back_calls_keep_their_own_inputs():
+    # consecutive host-buffer calls stage their inputs in alternating buffers on the
+    # context's copy stream; with no synchronisation between them each result must
+    # still be exactly the device-path result for its own input
+    w = inputs.Workload("host_pipe", T=700, d=512, d_ff=384, seed=17)
+    layer = inputs.make_layer(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    args = (layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
+    xs = [inputs.make_x(w, "cuda", seed=100 + i) for i in range(5)]
+    refs = [m.forward(x, *args).clone() for x in xs]
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty_like(h).pin_memory() for h in xh]
+    torch.cuda.synchronize()
+    for i in range(5):
+        m.forward_host(xh[i], *args, yh[i])
+    torch.cuda.synchronize()
+    assert m.status() == 0
+    for i in range(5):
+        assert torch.equal(yh[i], refs[i].cpu()), f"call {i}"
+
+
 # ----------------------------------------------------------------------------- Mixtral shape
 @pytest.fixture(scope="module")
 def mixtral_experts():
