@@ -73,8 +73,9 @@ typedef enum {
                                   CTA pairs -- tcgen05 cta_group::2, 256/128-row tiles -- when the device can
                                   co-schedule them), 1 = both single-CTA, 2 = both on CTA pairs or
                                   MOE_ERR_UNSUPPORTED */
-    MOE_OPT_HOST_OUTPUT = 6    /* moe_forward_host: 0 = copy y back on the stream (default), 1 = when y_host is
-                                  pinned, the layer's last kernel writes y into it directly over the bus */
+    MOE_OPT_HOST_OUTPUT = 6    /* moe_forward_host: 1 = when y_host is pinned, the layer's last kernel writes y
+                                  into it directly over the bus (default; measured 0.19 ms faster per call at
+                                  T=4096), 0 = always copy y back on the stream */
 } moe_option_t;
 
 /*
@@ -151,8 +152,10 @@ int moe_forward(moe_ctx* ctx, const void* x, const float* W_g, const void* W1, c
  * copies; pageable memory works but the copies then synchronise).  Copies x
  * to one of two context-owned device buffers on a stream of the context's own
  * (so that, with pinned memory, the copy overlaps the previous call's
- * kernels), runs the layer on `stream` once the copy is done, and copies y
- * back on `stream`.  Weights stay device pointers.  When `stream` reaches this
+ * kernels), runs the layer on `stream` once the copy is done, and -- when
+ * y_host is pinned -- lets the layer's last kernel write y straight into it
+ * (else y is copied back on `stream`; see MOE_OPT_HOST_OUTPUT).  Weights stay
+ * device pointers.  When `stream` reaches this
  * point, y_host holds the result; x_host must stay valid and unchanged until
  * then.  While `stream` is being captured into a graph, all of it runs on
  * `stream`.

@@ -19,7 +19,7 @@ struct moe_ctx {
     long long wait_limit_us = 2000000;
     int force_path = 0;
     int gemm_pair = 0;          // 0 auto, 1 single CTA, 2 CTA pairs
-    int host_out = 0;           // moe_forward_host: 1 = kernels write y into pinned host memory directly
+    int host_out = 1;           // moe_forward_host: 1 = kernels write y into pinned host memory directly
     int device = 0;
     int num_sms = 148;
     int* status_host = nullptr;   // host-mapped
@@ -163,7 +163,7 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->P2 = reinterpret_cast<float*>(b + L.P2);
     c->cap_T = T;
     c->cap_dec = Tdec;
-    if (cudaMemsetAsync(c->xchg, 0, L.rstd - L.xchg, s) != cudaSuccess) return MOE_ERR_CUDA;   // xchg + ccnt
+    if (cudaMemsetAsync(c->xchg, 0, L.rstd - L.xchg, s) != cudaSuccess) return MOE_ERR_CUDA;   // every counter region
     // Tensor maps of the workspace activations cover the full capacity; rows
     // beyond the live K*T are never valid rows of any tile.
     if (c->dtype == MOE_BF16) {

@@ -165,6 +165,26 @@ def test_host_entry_back_to_back_calls_keep_their_own_inputs():
         assert torch.equal(yh[i], refs[i].cpu()), f"call {i}"
 
 
+@pytest.mark.parametrize("pinned,direct", [(True, 1), (True, 0), (False, 1)])
+def test_host_entry_output_routes(pinned, direct):
+    # y written by the last kernel straight into pinned host memory, or copied back
+    # (pageable output, or the option off): all give the device path's result
+    w = inputs.Workload("host_out", T=300, d=512, d_ff=384, seed=19)
+    layer = inputs.make_layer(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    m.set_option(_lib.MOE_OPT_HOST_OUTPUT, direct)
+    args = (layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
+    ref = m.forward(layer["x"], *args).cpu()
+    xh = layer["x"].cpu()
+    yh = torch.empty_like(xh)
+    if pinned:
+        xh, yh = xh.pin_memory(), yh.pin_memory()
+    m.forward_host(xh, *args, yh)
+    torch.cuda.synchronize()
+    assert m.status() == 0
+    assert torch.equal(yh, ref)
+
+
 # ----------------------------------------------------------------------------- Mixtral shape
 @pytest.fixture(scope="module")
 def mixtral_experts():
