@@ -185,6 +185,32 @@ def test_host_entry_output_routes(pinned, direct):
     assert torch.equal(yh, ref)
 
 
+@pytest.mark.parametrize("T", [600, 40])
+def test_forward_replays_from_a_cuda_graph(T):
+    # the routing kernel's barrier words and the combine's counters return to zero
+    # after every call, so a captured call replays correctly; each replay must match
+    # an eager call on the same input bit for bit (grouped path at T=600, weight
+    # streaming at T=40)
+    w = inputs.Workload("graph", T=T, d=512, d_ff=384, seed=23 + T)
+    layer = inputs.make_layer(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    m.reserve(T)
+    args = (layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
+    x = layer["x"].clone()
+    y = torch.empty_like(x)
+    m.forward(x, *args, y=y)                 # outside capture: kernel attributes, device queries
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.forward(x, *args, y=y)
+    for i in range(3):
+        x.copy_(inputs.make_x(w, "cuda", seed=300 + i))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, m.forward(x, *args)), f"replay {i}"
+    assert m.status() == 0
+
+
 # ----------------------------------------------------------------------------- Mixtral shape
 @pytest.fixture(scope="module")
 def mixtral_experts():
