@@ -434,9 +434,10 @@ def time_oracle(x, Wg, W, budget_s: float, min_tokens: int, seed: int = 0):
     import oracle
     from sparse_mixture_experts_54_b300 import inputs
 
-    xo = inputs.to_oracle(x)
-    Wgo = inputs.to_oracle(Wg)
-    W1, W3, W2 = (inputs.to_oracle(t) for t in W)
+    # already host arrays when the caller converted them once (the reference arm)
+    xo = x if isinstance(x, np.ndarray) else inputs.to_oracle(x)
+    Wgo = Wg if isinstance(Wg, np.ndarray) else inputs.to_oracle(Wg)
+    W1, W3, W2 = (t if isinstance(t, np.ndarray) else inputs.to_oracle(t) for t in W)
     threads = oracle.max_threads()
     T = xo.shape[0]
     order = inputs.sample_tokens(T, T, seed).numpy()
@@ -469,13 +470,16 @@ def run_reference(args, rank, world):
     w = inputs.workload("prefill_t4096")
     # the oracle runs on the host: draw the inputs on the GPU when there is one (fast), then copy
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    W = inputs.make_experts(w, dev)
-    x = inputs.make_x(w, dev)
-    Wg, _ = inputs.make_router(w, dev)
+    W = tuple(inputs.to_oracle(t) for t in inputs.make_experts(w, dev))
+    x = inputs.to_oracle(inputs.make_x(w, dev))
+    Wg = inputs.to_oracle(inputs.make_router(w, dev)[0])
     per_step = []
     res = None
+    # each step is a bounded sample, sized so that the whole run stays within a few minutes
+    budget = args.ref_budget_s if args.ref_budget_s is not None else \
+        min(6.0, 150.0 / max(args.warmup + args.steps, 1))
     for i in range(args.warmup + args.steps):
-        res = time_oracle(x, Wg, W, budget_s=args.ref_budget_s, min_tokens=1, seed=i)
+        res = time_oracle(x, Wg, W, budget_s=budget, min_tokens=1, seed=i)
         if i >= args.warmup:
             per_step.append(res)
     tok_s = sum(r["tokens"] for r in per_step) / sum(r["seconds"] for r in per_step)
@@ -525,7 +529,8 @@ def main():
     ap.add_argument("--no-skewed", action="store_true", help="skip the skewed T=32768 measurement")
     ap.add_argument("--stack-passes", type=int, default=8)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
-    ap.add_argument("--ref-budget-s", type=float, default=6.0)
+    ap.add_argument("--ref-budget-s", type=float, default=None,
+                    help="oracle seconds per reference step (default: min(6, 150 / (warmup + steps)))")
     ap.add_argument("--profile-step", default=None, help="workload name: run warmup+1 untimed calls (for ncu)")
     ap.add_argument("--force-path", type=int, default=0)
     args = ap.parse_args()

@@ -54,6 +54,8 @@ SMALL_BF16 = [
     (300, 256, 256, 4, 1),
     (257, 256, 256, 8, 3),
     (200, 768, 640, 16, 2),
+    (200, 256, 256, 8, 8),      # K = n: dense routing, every token to every expert
+    (150, 256, 256, 2, 2),      # two experts, both taken
 ]
 
 
@@ -267,6 +269,7 @@ DECODE_CASES = [
     (77, 256, 384, 8, 3),
     (120, 768, 640, 16, 2),
     (256, 256, 256, 8, 2),
+    (16, 256, 256, 8, 8),       # K = n on the weight-streaming path
 ]
 
 
