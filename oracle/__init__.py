@@ -233,3 +233,26 @@ def block_forward(h: np.ndarray, Wg, W1, W3, W2, K: int, eps: float, bias=None, 
     y = moe_tokens(u, W1, W3, W2, idx, gate, np.arange(u.shape[0]), nthreads)
     h_new = widen(h) + y
     return dict(u=u, logits=logits, idx=idx, gate=gate, y=y, h_new=h_new, h_bits=_store_like(h_new, h))
+
+
+# --------------------------------------------------------------------------- fp8 expert weights
+# Not part of the method on the pages: an input format of the library's
+# fp8-weight entry point.  A weight is scale[row] * q, q an OCP e4m3 byte.
+
+def decode_e4m3(q: np.ndarray) -> np.ndarray:
+    """Exact fp64 value of OCP FP8 E4M3 bytes (uint8): sign bit, 4 exponent bits
+    with bias 7, 3 mantissa bits; exponent field 0 is subnormal (M/8 * 2^-6);
+    the all-ones pattern S.1111.111 is NaN (the format has no infinities)."""
+    q = np.asarray(q, dtype=np.uint8)
+    sign = np.where(q & 0x80, -1.0, 1.0)
+    E = ((q >> 3) & 0xF).astype(np.int64)
+    M = (q & 0x7).astype(np.float64)
+    normal = np.ldexp(1.0 + M / 8.0, E - 7)
+    sub = np.ldexp(M / 8.0, -6)
+    v = sign * np.where(E == 0, sub, normal)
+    return np.where((E == 15) & (M == 7), np.nan, v)
+
+
+def dequantize_e4m3_rows(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """W[..., r, j] = scale[..., r] * e4m3(q[..., r, j]) in fp64."""
+    return np.asarray(scale, dtype=np.float64)[..., None] * decode_e4m3(q)

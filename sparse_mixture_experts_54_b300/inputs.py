@@ -165,3 +165,32 @@ def sample_tokens(T: int, count: int, seed: int = 0) -> torch.Tensor:
     g = torch.Generator(device="cpu")
     g.manual_seed(seed + 12345)
     return torch.randperm(T, generator=g)[:count].sort().values
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3_rows(W: torch.Tensor):
+    """fp8 expert weights for ``moe_forward_fp8``: per weight row (last axis
+    reduced) the smallest power-of-two scale s with max|W_row| / s <= 448, and
+    q = e4m3(W_row / s) (torch's round-to-nearest cast; the division is exact).
+    Returns (q as torch.uint8 bytes, s as float32), on W's device.  Rows of zeros
+    get s = 1.  With power-of-two scales the dequantised weights s * q are exact
+    in bf16, so the fp8 path can be checked against the bf16 path bit for bit."""
+    Wf = W.float()
+    amax = Wf.abs().amax(dim=-1)
+    m, e = torch.frexp(amax / E4M3_MAX)          # amax / 448 = m * 2^e, 0.5 <= m < 1
+    e = torch.where(m == 0.5, e - 1, e)          # an exact power of two needs no round-up
+    s = torch.where(amax > 0, torch.ldexp(torch.ones_like(amax), e), torch.ones_like(amax))
+    q = (Wf / s[..., None]).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), s.contiguous()
+
+
+def dequantize_e4m3_rows(q: torch.Tensor, s: torch.Tensor, dtype=torch.bfloat16) -> torch.Tensor:
+    """s[..., None] * e4m3(q) in ``dtype`` (exact in bf16 for power-of-two s)."""
+    return (s[..., None] * q.view(torch.float8_e4m3fn).float()).to(dtype)
+
+
+def every_e4m3_code(device="cpu") -> torch.Tensor:
+    """The 254 non-NaN e4m3 bytes, ascending: zeros, subnormals, normals, both signs."""
+    return torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8, device=device)
