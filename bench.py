@@ -270,6 +270,9 @@ def run_ours(args, rank, world, dist):
     barrier(dist)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)
 
+    # decode with fp8 (e4m3) expert weights, power-of-two row scales
+    fp8 = run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist) if not args.no_fp8 else None
+
     alg_p = algorithmic(wp.T, counts_p)
     alg_d = algorithmic(wd.T, counts_d)
     tok_s = world * wp.T / (ms_p * 1e-3)
@@ -309,6 +312,7 @@ def run_ours(args, rank, world, dist):
         "instrumented_ms_per_step": {"prefill": round(ms_pi, 4), "decode": round(ms_di, 4)},
         "roofline": roofline,
         "skewed_t32768": skew,
+        "decode_fp8": fp8,
         "e2e": {"value": round(world * wp.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                 "d2h_bytes_per_step": int(yh.numel() * yh.element_size()),
@@ -327,6 +331,64 @@ def run_ours(args, rank, world, dist):
     if not args.no_stack:
         line["stack32"] = run_stack(args, dist)
     return line, host
+
+
+def run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist):
+    """Decode batches through moe_forward_fp8: the same experts quantised to e4m3
+    with one power-of-two scale per weight row (1.41 GB of weight bytes instead
+    of 2.82 GB), the same router.  Back-to-back calls, CUDA events."""
+    from sparse_mixture_experts_54_b300 import _lib, inputs
+
+    q, s = {}, {}
+    for name, t in (("W1", W1), ("W3", W3), ("W2", W2)):
+        q[name], s[name] = inputs.quantize_e4m3_rows(t)
+    args8 = (q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
+    stream = torch.cuda.current_stream()
+    w = inputs.workload("decode_t32")
+    out = {"weights": "e4m3, one fp32 power-of-two scale per weight row", "us_per_layer": {}}
+
+    def timed(T, steps, stage_timing):
+        x = inputs.make_x(w, "cuda", seed=17, T=T)
+        y = torch.empty((T, w.d), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup):
+            m.forward_fp8(x, Wg, *args8, y=y)
+        torch.cuda.synchronize()
+        m.set_option(_lib.MOE_OPT_STAGE_TIMING, 1 if stage_timing else 0)
+        m.stage_times()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            m.forward_fp8(x, Wg, *args8, y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        stages, _ = m.stage_times()
+        m.set_option(_lib.MOE_OPT_STAGE_TIMING, 0)
+        assert m.status() == 0, _lib.moe_error_string(m.status())
+        counts = m.route(x, Wg)["counts"].cpu().tolist()
+        return max_over_ranks(e0.elapsed_time(e1) / steps, dist), stages, counts
+
+    ms, _, counts = timed(32, args.decode_steps, False)
+    _, stages, _ = timed(32, max(args.decode_steps // 2, 3), True)
+    touched = sum(1 for c in counts if c > 0)
+    wbytes = touched * (3 * w.d * w.d_ff + (2 * w.d_ff + w.d) * 4)   # e4m3 bytes + row scales
+    nbytes = wbytes + 2 * 32 * w.d * 2 + w.n_experts * w.d * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["decode_t32"] = {"us_per_layer": round(ms * 1e3, 1), "weight_gbytes": round(wbytes / 1e9, 3),
+                         "experts_touched": touched, "achieved_gbs": round(gbs, 1),
+                         "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                         "stages_us": {k: round(v * 1e3, 1) for k, v in stages.items()},
+                         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                                      "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                                      "bytes_per_step": int(nbytes)}}
+    for T in (1, 8, 128, 256):
+        ms_t, _, _ = timed(T, max(args.decode_steps // 4, 20), False)
+        out["us_per_layer"][str(T)] = round(ms_t * 1e3, 1)
+    out["us_per_layer"]["32"] = round(ms * 1e3, 1)
+    del q, s, args8
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_skewed(args, W1, W3, W2, pk, dist):
@@ -527,6 +589,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack measurement")
     ap.add_argument("--no-skewed", action="store_true", help="skip the skewed T=32768 measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-weight decode measurements")
     ap.add_argument("--stack-passes", type=int, default=8)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=None,

@@ -190,6 +190,37 @@ int moe_stack_forward(moe_ctx* ctx, void* h, float eps, int n_layers, const floa
                       const void* const* W1, const void* const* W3, const void* const* W2, int T,
                       moe_stream_t stream);
 
+/*
+ * moe_forward with fp8 expert weights, for decode-sized batches: y [T][d] =
+ * MoE(x) with
+ *     W1_i[f][j] = W1_scale[i][f] * W1q[i][f][j]     (same for W3; W2 per d row)
+ * where W1q, W3q, W2q hold OCP e4m3 bytes (1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits; 0x7F/0xFF (NaN) are not accepted and give unspecified
+ * results) in the layouts of W1, W3, W2 above, and the scales are fp32, one
+ * per weight row: W1_scale, W3_scale [n][d_ff], W2_scale [n][d].  Fp8 weights
+ * are not part of the method as the pages give it; they halve the bytes a
+ * weight-streaming layer reads (the layer's decode time is the time to read
+ * the touched experts' weights).
+ *
+ * Computation: the weight-streaming kernels of moe_forward's small-T path, the
+ * weight tiles widened exactly to bf16 on chip and the row scale applied to the
+ * fp32 accumulator.  When every scale is a power of two (including 1) the
+ * result is bitwise identical to moe_forward on the bf16 weights
+ * scale * q (which are exact in bf16); other scales are also exact to fp32
+ * rounding of one product per partial sum.
+ *
+ * Requirements: bf16 context; d a multiple of 256 and d_ff of 128 (as
+ * moe_forward's bf16 path); n <= 31.  x, y, W_g device as moe_forward; W1q,
+ * W3q, W2q device, 16-byte aligned; the scales device, 4-byte aligned.
+ * Batches of more than 256 tokens run as consecutive 256-token chunks on
+ * `stream` (each chunk reads every touched expert's weights once).  Errors
+ * and asynchrony as moe_forward; per-kernel times through moe_stage_times
+ * with the same four stages.
+ */
+int moe_forward_fp8(moe_ctx* ctx, const void* x, const float* W_g, const uint8_t* W1q,
+                    const float* W1_scale, const uint8_t* W3q, const float* W3_scale,
+                    const uint8_t* W2q, const float* W2_scale, void* y, int T, moe_stream_t stream);
+
 /* Sticky kernel-side status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_BOUNDS) of every
  * call so far; reads host-mapped memory, synchronises nothing.  Results written
  * by kernels still running are not yet visible. */

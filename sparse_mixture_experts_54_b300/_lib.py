@@ -50,6 +50,7 @@ SIGNATURES = {
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_block_forward": (_I, [_P, _P, ctypes.c_float, _P, _P, _P, _P, _I, _P]),
     "moe_stack_forward": (_I, [_P, _P, ctypes.c_float, _I, _P, _P, _P, _P, _I, _P]),
+    "moe_forward_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_status": (_I, [_P]),
     "moe_clear_status": (_I, [_P]),
     "moe_selftest_wait_timeout": (_I, [_P, _LL, _P]),
@@ -151,6 +152,11 @@ def moe_stack_forward(ctx, h, eps, n_layers, W_g, W1, W3, W2, T, stream) -> int:
     """W_g, W1, W3, W2: addresses of host arrays of n_layers device pointers."""
     return load().moe_stack_forward(ctx, _p(h), float(eps), n_layers, _p(W_g), _p(W1), _p(W3), _p(W2), T,
                                     _p(stream))
+
+
+def moe_forward_fp8(ctx, x, W_g, W1q, W1_scale, W3q, W3_scale, W2q, W2_scale, y, T, stream) -> int:
+    return load().moe_forward_fp8(ctx, _p(x), _p(W_g), _p(W1q), _p(W1_scale), _p(W3q), _p(W3_scale), _p(W2q),
+                                  _p(W2_scale), _p(y), T, _p(stream))
 
 
 def moe_status(ctx) -> int:

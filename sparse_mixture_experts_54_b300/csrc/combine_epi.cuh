@@ -75,7 +75,6 @@ __device__ __forceinline__ void combine_arrive(const CombineArgs& c, const float
                 }
             }
         }
-#pragma unroll
         if (c.resid) {
             // residual stream: y = h + (sum of the slot rows), one rounding
 #pragma unroll

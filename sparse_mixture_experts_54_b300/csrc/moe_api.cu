@@ -359,6 +359,43 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
     return MOE_OK;
 }
 
+// y = MoE(x) for T <= kDecodeMaxT tokens with e4m3 expert weights and fp32
+// row scales: the weight-streaming path with the fp8 GEMM kernels, same split
+// choice, SwiGLU and combine kernels as the bf16 one.
+int run_forward_fp8(moe_ctx* c, const void* x, const float* Wg, const uint8_t* W1q, const float* W1s,
+                    const uint8_t* W3q, const float* W3s, const uint8_t* W2q, const float* W2s, void* y, int T,
+                    cudaStream_t s) {
+    const int R = c->k * T;
+    StageMarks marks(c, s);
+    int rc = run_route(c, x, Wg, T, s, nullptr, true);
+    if (rc != MOE_OK) return rc;
+    marks.mark(0);
+    CUtensorMap mW1, mW3, mW2;
+    const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
+    if (!encode_map_u8_2d(&mW1, W1q, nF, c->d, 64, 128) || !encode_map_u8_2d(&mW3, W3q, nF, c->d, 64, 128) ||
+        !encode_map_u8_2d(&mW2, W2q, nd, c->F, 64, 128))
+        return MOE_ERR_CUDA;
+    const KStatus st = kstatus(c);
+    const int touched = c->n < R ? c->n : R;
+    const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 64, c->num_sms);
+    const int s1 = decode_pick_splits(touched * (c->d / 128), c->F / 64, c->num_sms);
+    cudaError_t e = launch_decode_fp8_w13(mW1, mW3, c->map_Xp32, W1s, W3s, c->sched, c->n, c->d, c->F, T, c->k, s0,
+                                          c->Pa, c->Pb, st, c->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(1);
+    e = launch_decode_fp8_w2(mW2, c->map_H32, W2s, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms,
+                             s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(2);
+    e = launch_decode_combine(ElemType::BF16, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, nullptr, y, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.mark(3);
+    marks.finish();
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -539,6 +576,30 @@ int moe_stack_forward(moe_ctx* c, void* h, float eps, int n_layers, const float*
     int rc = ensure_workspace(c, T, s, use_decode(c, T));
     if (rc != MOE_OK) return rc;
     for (int l = 0; l < n_layers && rc == MOE_OK; ++l) rc = run_forward(c, h, Wg[l], W1[l], W3[l], W2[l], h, T, s, eps, h);
+    return rc;
+}
+
+int moe_forward_fp8(moe_ctx* c, const void* x, const float* Wg, const uint8_t* W1q, const float* W1s,
+                    const uint8_t* W3q, const float* W3s, const uint8_t* W2q, const float* W2s, void* y, int T,
+                    moe_stream_t stream) {
+    if (!c || T < 0) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    if (!x || !Wg || !W1q || !W1s || !W3q || !W3s || !W2q || !W2s || !y) return MOE_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1q) || !aligned16(W3q) || !aligned16(W2q) || !aligned16(y))
+        return MOE_ERR_INVALID;
+    auto aligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+    if (!aligned4(W1s) || !aligned4(W3s) || !aligned4(W2s)) return MOE_ERR_INVALID;
+    if (c->dtype != MOE_BF16 || !tc_shape_ok(c) || c->n > 31) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int chunk = T < kDecodeMaxT ? T : kDecodeMaxT;
+    int rc = ensure_workspace(c, chunk, s, true);
+    if (rc != MOE_OK) return rc;
+    const size_t row_bytes = static_cast<size_t>(c->d) * 2;
+    for (int t0 = 0; t0 < T && rc == MOE_OK; t0 += chunk) {
+        const int Tc = T - t0 < chunk ? T - t0 : chunk;
+        rc = run_forward_fp8(c, static_cast<const char*>(x) + t0 * row_bytes, Wg, W1q, W1s, W3q, W3s, W2q, W2s,
+                             static_cast<char*>(y) + t0 * row_bytes, Tc, s);
+    }
     return rc;
 }
 

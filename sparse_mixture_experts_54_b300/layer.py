@@ -106,6 +106,25 @@ class MoELayer:
                                          _stream_handle(stream)), "moe_forward_host")
         return y_host
 
+    def forward_fp8(self, x, Wg, W1q, W1_scale, W3q, W3_scale, W2q, W2_scale, y: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+        """y = MoE(x) with e4m3 expert weights (torch.float8_e4m3fn or their bytes as torch.uint8)
+        and fp32 row scales: W1 = W1_scale[..., None] * W1q, likewise W3 and W2 (bf16 layers only)."""
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.d), dtype=self.dtype, device=x.device)
+        q = {}
+        for name, t in (("W1q", W1q), ("W3q", W3q), ("W2q", W2q)):
+            if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+                raise ValueError(f"{name} must be torch.float8_e4m3fn or torch.uint8, got {t.dtype}")
+            q[name] = _dev_ptr(t, None, name)
+        _lib.check(_lib.moe_forward_fp8(self.ctx, _dev_ptr(x, self.dtype, "x"), _dev_ptr(Wg, torch.float32, "W_g"),
+                                        q["W1q"], _dev_ptr(W1_scale, torch.float32, "W1_scale"),
+                                        q["W3q"], _dev_ptr(W3_scale, torch.float32, "W3_scale"),
+                                        q["W2q"], _dev_ptr(W2_scale, torch.float32, "W2_scale"),
+                                        _dev_ptr(y, self.dtype, "y"), T, _stream_handle(stream)), "moe_forward_fp8")
+        return y
+
     def block_forward(self, h: torch.Tensor, Wg, W1, W3, W2, eps: float = 1e-5, stream=None) -> torch.Tensor:
         """In place: h <- h + MoE(RMSNorm(h)) (one residual block of a stack)."""
         T = h.shape[0]
