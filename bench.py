@@ -572,8 +572,14 @@ def profile_step(args):
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=b)
     if args.force_path:
         m.set_option(_lib.MOE_OPT_FORCE_PATH, args.force_path)
-    for _ in range(args.warmup + 1):
-        m.forward(x, Wg, W1, W3, W2)
+    if args.fp8:
+        q = [inputs.quantize_e4m3_rows(t) for t in (W1, W3, W2)]
+        del W1, W3, W2
+        for _ in range(args.warmup + 1):
+            m.forward_fp8(x, Wg, q[0][0], q[0][1], q[1][0], q[1][1], q[2][0], q[2][1])
+    else:
+        for _ in range(args.warmup + 1):
+            m.forward(x, Wg, W1, W3, W2)
     torch.cuda.synchronize()
     assert m.status() == 0
     print(f"profile_step {w.name}: {args.warmup + 1} forward calls done", flush=True)
@@ -590,6 +596,7 @@ def main():
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack measurement")
     ap.add_argument("--no-skewed", action="store_true", help="skip the skewed T=32768 measurement")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-weight decode measurements")
+    ap.add_argument("--fp8", action="store_true", help="with --profile-step: fp8 expert weights (moe_forward_fp8)")
     ap.add_argument("--stack-passes", type=int, default=8)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=None,

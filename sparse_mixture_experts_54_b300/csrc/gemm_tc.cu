@@ -346,18 +346,18 @@ bool encode_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint6
     return r == CUDA_SUCCESS;
 }
 
-// Row-major byte matrix [rows][cols] -> tensor map with a (box_cols x box_rows)
-// box, no swizzle, zero fill outside the matrix.
-bool encode_map_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                      uint32_t box_rows) {
+// Row-major byte matrix [rows][cols] (cols a multiple of 64) -> tensor map
+// with a (64-byte x 128-row) box and 64-byte swizzle: 16-byte chunk c of box
+// row r lands at chunk c ^ ((r / 2) % 4) of that row.
+bool encode_map_u8_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
     auto fn = encode_fn();
     if (!fn || rows == 0 || cols == 0) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
-    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t box[2] = {64, 128};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

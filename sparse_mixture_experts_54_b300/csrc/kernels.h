@@ -112,11 +112,10 @@ cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R,
 cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
                                   int T, int K, int d, const void* resid, void* y, cudaStream_t s);
 
-// the same with e4m3 weights and fp32 row scales (decode_fp8.cu); the maps
-// come from encode_map_u8_2d with a (64 x 128) box, the partial sums feed
-// launch_decode_swiglu / launch_decode_combine unchanged
-bool encode_map_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                      uint32_t box_rows);
+// the same with e4m3 weights and fp32 row scales (decode_fp8.cu); the weight
+// maps come from encode_map_u8_sw64, the partial sums feed launch_decode_swiglu /
+// launch_decode_combine unchanged
+bool encode_map_u8_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 cudaError_t launch_decode_fp8_w13(const CUtensorMap& mapW1q, const CUtensorMap& mapW3q, const CUtensorMap& mapXp32,
                                   const float* W1s, const float* W3s, const int* sched, int n, int d, int F, int T,
                                   int K, int splits, float* Pa, float* Pb, KStatus st, int num_sms, cudaStream_t s);

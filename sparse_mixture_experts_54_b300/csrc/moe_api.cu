@@ -372,8 +372,8 @@ int run_forward_fp8(moe_ctx* c, const void* x, const float* Wg, const uint8_t* W
     marks.mark(0);
     CUtensorMap mW1, mW3, mW2;
     const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
-    if (!encode_map_u8_2d(&mW1, W1q, nF, c->d, 64, 128) || !encode_map_u8_2d(&mW3, W3q, nF, c->d, 64, 128) ||
-        !encode_map_u8_2d(&mW2, W2q, nd, c->F, 64, 128))
+    if (!encode_map_u8_sw64(&mW1, W1q, nF, c->d) || !encode_map_u8_sw64(&mW3, W3q, nF, c->d) ||
+        !encode_map_u8_sw64(&mW2, W2q, nd, c->F))
         return MOE_ERR_CUDA;
     const KStatus st = kstatus(c);
     const int touched = c->n < R ? c->n : R;
