@@ -94,6 +94,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const K
     return false;
 }
 
+// Whole-warp forms, for warps that go on to warp-collective (.sync.aligned)
+// tcgen05 instructions: lane 0 polls, the outcome is broadcast, and the warp
+// leaves converged, so every lane reaches the same tcgen05.ld/st instruction.
+// The shuffle orders lane 0's acquire before the other lanes' later accesses.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const KStatus& st,
+                                               const volatile int* abort_flag) {
+    __syncwarp();
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, st, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok != 0;
+}
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor loads into shared memory, completion on an mbarrier)
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -290,6 +302,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         }
     }
     return false;
+}
+// mbar_wait_cluster for a whole warp (see mbar_wait_warp).
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, const KStatus& st,
+                                                       const volatile int* abort_flag) {
+    __syncwarp();
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_cluster(bar, parity, st, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok != 0;
 }
 // 2-D tile load into this CTA's shared memory whose completion is counted on
 // an mbarrier of either CTA of the pair (cluster-window address).

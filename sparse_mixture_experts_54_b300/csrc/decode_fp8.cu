@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(Q8_THREADS, 1)
         bool ok = true;
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             for (int k = 0; k < p.kb_per_split; ++k) {
-                if (!mbar_wait(full_bar(stage), phase, st, abort_flag)) { ok = false; break; }
-                if (!mbar_wait(aempty_bar(ast), aph ^ 1u, st, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_warp(full_bar(stage), phase, st, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_warp(aempty_bar(ast), aph ^ 1u, st, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint8_t* src = ring_ptr + stage * stage_bytes;
                 const uint32_t acol = static_cast<uint32_t>(a_col0 + ast * a_cols);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1)
             const int off = offsets[e];
             const int feat = rb * 128 + q * 32 + lane;   // this thread's weight row = output feature
             const size_t srow = static_cast<size_t>(e) * p.rows_per_e + feat;
-            if (!mbar_wait(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t t0 =
                 tmem_base + static_cast<uint32_t>(acc * acc_stride) + (static_cast<uint32_t>(q * 32) << 16);
@@ -425,15 +425,17 @@ __global__ void __launch_bounds__(Q8_THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 
+namespace {
 template <int MODE>
-static cudaError_t launch_fp8(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, Fp8DecArgs args,
-                              int num_sms, cudaStream_t s) {
+cudaError_t launch_fp8(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, Fp8DecArgs args,
+                       int num_sms, cudaStream_t s) {
     auto kern = tc_decode_fp8_kernel<MODE>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Q8_SMEM_BYTES));
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(num_sms), dim3(Q8_THREADS), Q8_SMEM_BYTES, s, a0, a1, b, args);
 }
+}  // namespace
 
 cudaError_t launch_decode_fp8_w13(const CUtensorMap& mapW1q, const CUtensorMap& mapW3q, const CUtensorMap& mapXp32,
                                   const float* W1s, const float* W3s, const int* sched, int n, int d, int F, int T,

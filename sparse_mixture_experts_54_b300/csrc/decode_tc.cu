@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             const int N = item_n(e);
             const int cnt = counts[e];
             const int off = offsets[e];
-            if (!mbar_wait(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const int feat = rb * 128 + q * 32 + lane;   // this thread's weight row = output feature
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;

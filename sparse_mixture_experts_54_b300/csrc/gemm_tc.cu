@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             int e, mb, nb;
             tc_decode_tile(prefix, n, p.ntiles, p.group_m, tile, e, mb, nb);
-            if (!mbar_wait(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const int rloc = mb * BM + q * 32 + lane;      // row inside the expert
             const bool valid = rloc < counts[e];

@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             int e, mb, nb;
             bool half;
             pair_decode_tile(prefix, counts, n, p.ntiles, p.group_m, tile, e, mb, nb, half);
-            if (!mbar_wait_cluster(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_cluster_warp(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
             // Full tile: lane L of this CTA's tensor memory is tile row 128*rank + L,
             // all 256 columns.  128-row tile: lane L is tile row 64*rank + (L % 64),

@@ -85,6 +85,7 @@ def test_fp8_equals_bf16_on_dequantised_weights(T, d, F, n, K):
 
 
 def test_fp8_all_tokens_to_one_expert_pair_and_deterministic():
+    # 200 tokens on experts (5, 2): N = 224 token columns per item; W1 and W3 run as separate items
     w = inputs.Workload("fp8_skew", T=200, d=256, d_ff=384, bias=(0, 0, 50, 0, 0, 100, 0, 0), seed=8)
     layer = inputs.make_layer(w, "cuda")
     q, s = quantize_layer(layer)
@@ -166,7 +167,6 @@ def test_mixtral_decode_t32_fp8(mixtral_fp8):
     w, q, s = mixtral_fp8
     x = inputs.make_x(w, "cuda")
     Wg, b = inputs.make_router(w, "cuda")
-    layer = dict(x=x, Wg=Wg, bias=b)
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=b)
     r = m.route(x, Wg)
     y8 = m.forward_fp8(x, Wg, q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
