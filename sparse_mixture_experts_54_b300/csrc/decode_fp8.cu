@@ -89,14 +89,19 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 }
 
 // Four e4m3 bytes (element order: low byte first) -> four bf16 in two words.
+// With the whole bytes at bytes 1 and 3 (f = b0 << 8 | b1 << 24) and the
+// magnitudes at bytes 0 and 2 (m = (b0 & 0x7f) | (b1 & 0x7f) << 16),
+// f - 240 m = (b0 & 0x80) << 8 | (b0 & 0x7f) << 4 | (the same for b1) << 16:
+// each sign at bit 15, each magnitude at bits 4..10, no borrow between the
+// halves (checked for all byte pairs) -- one multiply-add instead of a mask,
+// a shift and an OR.
 __device__ __forceinline__ void widen_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     constexpr uint32_t kTwo120 = 0x7B807B80u;   // bf16 2^120 in both halves
-    const uint32_t mag = w & 0x7F7F7F7Fu, sgn = w & 0x80808080u;
-    // magnitudes to bytes 0 and 2 (shifted up by 4 below), signs to bytes 1 and 3
-    const uint32_t m01 = __byte_perm(mag, 0u, 0x4140), s01 = __byte_perm(sgn, 0u, 0x1404);
-    const uint32_t m23 = __byte_perm(mag, 0u, 0x4342), s23 = __byte_perm(sgn, 0u, 0x3424);
-    lo = mul_bf16x2(m01 * 16u + s01, kTwo120);
-    hi = mul_bf16x2(m23 * 16u + s23, kTwo120);
+    const uint32_t mag = w & 0x7F7F7F7Fu;
+    const uint32_t m01 = __byte_perm(mag, 0u, 0x4140), f01 = __byte_perm(w, 0u, 0x1404);
+    const uint32_t m23 = __byte_perm(mag, 0u, 0x4342), f23 = __byte_perm(w, 0u, 0x3424);
+    lo = mul_bf16x2(f01 - 240u * m01, kTwo120);
+    hi = mul_bf16x2(f23 - 240u * m23, kTwo120);
 }
 
 __device__ __forceinline__ void widen_chunk(const uint4& v, uint32_t* o) {
@@ -334,9 +339,9 @@ __global__ void __launch_bounds__(Q8_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * acc_stride);
                 for (int k = 0; k < p.kb_per_split; ++k) {
+                    // The converters arrive on afull only after they saw this stage's
+                    // full barrier complete, so the token rows' TMA has landed too.
                     if (!mbar_wait(afull_bar(ast), aph, st, abort_flag)) { ok = false; break; }
-                    // the token rows' TMA completed on this stage's full barrier
-                    if (!mbar_wait(full_bar(stage), phase, st, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = tmem_base + static_cast<uint32_t>(a_col0 + ast * a_cols);
                     const uint64_t bdesc =
