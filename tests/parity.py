@@ -1,6 +1,9 @@
 """Comparison helpers shared by the GPU parity tests (test-side logic only).
 
-Tolerances (from the layer's arithmetic):
+Tolerances, derived from the layer's arithmetic: fp32 accumulation over K = d
+or d_ff products of bf16 operands, with the SwiGLU product H rounded once to
+bf16 before the W2 GEMM, so the expected relative error of y is a few bf16 ulps
+(2^-8) spread over d_ff terms, well inside 1e-2 of the output's RMS:
   * routing indices and dispatch order: bit-exact, except near-tie tokens whose
     fp64 oracle logits have two neighbours among the top K+1 closer than 1e-6
     (fp32 on the GPU may order them either way); those are counted;
