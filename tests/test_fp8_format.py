@@ -86,3 +86,25 @@ def test_quantizer_scales_range_and_error():
     assert np.all(np.abs(deq - W64) <= bound)
     # the torch-side dequantisation equals the oracle's (both exact)
     assert np.array_equal(inputs.dequantize_e4m3_rows(q, s, torch.float32).double().numpy(), deq)
+
+
+def test_widening_recipe_against_the_format():
+    """The fp8 kernels widen a byte pair (b0, b1) to two bf16 with integer steps:
+    f = b0 << 8 | b1 << 24, m = (b0 & 0x7f) | (b1 & 0x7f) << 16, r = f - 240 m
+    (mod 2^32), each 16-bit half of r read as bf16 and multiplied by 2^120.  Here
+    that recipe, restated on the host for every pair of finite codes, must give
+    the oracle's decoding of the bytes exactly (zeros and subnormals included)."""
+    codes = inputs.every_e4m3_code().numpy().astype(np.uint32)
+    b0, b1 = np.meshgrid(codes, codes, indexing="ij")
+    b0, b1 = b0.ravel(), b1.ravel()
+    f = (b0 << 8) | (b1 << 24)
+    m = (b0 & 0x7F) | ((b1 & 0x7F) << 16)
+    r = (f - np.uint32(240) * m) & np.uint32(0xFFFFFFFF)
+    lo = (r & 0xFFFF).astype(np.uint32) << 16          # bf16 bits -> fp32 bits
+    hi = (r >> 16).astype(np.uint32) << 16
+    v_lo = lo.view(np.float32).astype(np.float64) * 2.0 ** 120
+    v_hi = hi.view(np.float32).astype(np.float64) * 2.0 ** 120
+    assert np.array_equal(v_lo, oracle.decode_e4m3(b0.astype(np.uint8)))
+    assert np.array_equal(v_hi, oracle.decode_e4m3(b1.astype(np.uint8)))
+    # the sign of zero survives too
+    assert np.array_equal(np.signbit(v_lo), np.signbit(oracle.decode_e4m3(b0.astype(np.uint8))))
