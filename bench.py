@@ -143,8 +143,8 @@ class ClockSampler:
         while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout_s:
             time.sleep(0.05)
 
-    def window(self, t0: float, t1: float):
-        self.windows.append((t0, t1))
+    def window(self, t0: float, t1: float, name: str = "headline"):
+        self.windows.append((name, t0, t1))
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -154,10 +154,12 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, which=("headline",)):
+        """Clock record of the samples inside the named timed windows."""
         sm, smax, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        inside = [l for (t, l) in self.lines if any(a <= t <= b + 0.25 for a, b in self.windows)]
+        wins = [(a, b) for (n, a, b) in self.windows if n in which]
+        inside = [l for (t, l) in self.lines if any(a <= t <= b + 0.25 for a, b in wins)]
         for line in inside:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
@@ -171,7 +173,7 @@ class ClockSampler:
             for name, flag in zip(names, parts[4:8]):
                 if flag.lower() == "active":
                     reasons.add(name)
-        timed_s = sum(b - a for a, b in self.windows)
+        timed_s = sum(b - a for a, b in wins)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "timed_seconds": round(timed_s, 3), "note": "no nvidia-smi sample inside the timed region"}
@@ -192,6 +194,32 @@ def algorithmic(T: int, counts, d=4096, F=14336, n=8, k=2):
                 bytes=w_bytes + act_bytes, weight_bytes=w_bytes, touched=touched)
 
 
+class L2Flush:
+    """Writes a buffer twice the size of L2 (126 MB) so that the next call reads its
+    weights from HBM."""
+
+    def __init__(self, nbytes: int = 256 << 20):
+        self.buf = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def timed_per_call(fn, steps: int, stream, flush=None):
+    """Mean ms of fn() over `steps` calls, each bracketed by its own CUDA events on
+    the stream; with `flush`, L2 is overwritten before each call (outside the
+    events)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev:
+        if flush is not None:
+            flush()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.fmean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+
 def run_ours(args, rank, world, dist):
     from sparse_mixture_experts_54_b300 import _lib, inputs
     from sparse_mixture_experts_54_b300.layer import MoELayer
@@ -207,18 +235,20 @@ def run_ours(args, rank, world, dist):
     m = MoELayer(wp.d, wp.d_ff, wp.n_experts, wp.k)
     m.reserve(wp.T)
     stream = torch.cuda.current_stream()
+    flush = L2Flush()
+    yp = torch.empty((wp.T, wp.d), dtype=torch.bfloat16, device="cuda")
+    yd = torch.empty((wd.T, wd.d), dtype=torch.bfloat16, device="cuda")
 
-    def timed(x, steps, warmup, stage_timing, clk=None):
+    def timed(x, y, steps, warmup, stage_timing, clk=None, window=None):
         """Mean ms per call over `steps` back-to-back calls (CUDA events on the stream).
 
         With stage_timing the library also records events around each kernel;
-        those calls give the per-kernel breakdown (and cost a little launch overlap)."""
+        those calls give the per-kernel breakdown."""
         for _ in range(warmup):
-            m.forward(x, Wg, W1, W3, W2)
+            m.forward(x, Wg, W1, W3, W2, y=y)
         torch.cuda.synchronize()
         m.set_option(_lib.MOE_OPT_STAGE_TIMING, 1 if stage_timing else 0)
         m.stage_times()   # drop warm-up records
-        y = torch.empty((x.shape[0], wp.d), dtype=torch.bfloat16, device="cuda")
         barrier(dist)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -229,7 +259,7 @@ def run_ours(args, rank, world, dist):
         e1.record(stream)
         torch.cuda.synchronize()
         if clk is not None:
-            clk.window(t0, time.monotonic())
+            clk.window(t0, time.monotonic(), window)
         barrier(dist)
         ms = e0.elapsed_time(e1) / steps
         stages, calls = m.stage_times()
@@ -237,19 +267,48 @@ def run_ours(args, rank, world, dist):
         assert m.status() == 0, _lib.moe_error_string(m.status())
         return max_over_ranks(ms, dist), stages
 
-    # routing statistics of the prefill batch (for the algorithmic byte count)
+    def timed_decode(steps, stage_timing, clk=None, window=None):
+        """Decode calls, L2 flushed before each one, CUDA events around each call."""
+        for _ in range(args.warmup):
+            m.forward(xd, Wg, W1, W3, W2, y=yd)
+        torch.cuda.synchronize()
+        m.set_option(_lib.MOE_OPT_STAGE_TIMING, 1 if stage_timing else 0)
+        m.stage_times()
+        barrier(dist)
+        t0 = time.monotonic()
+        ms = timed_per_call(lambda: m.forward(xd, Wg, W1, W3, W2, y=yd), steps, stream, flush)
+        if clk is not None:
+            clk.window(t0, time.monotonic(), window)
+        barrier(dist)
+        stages, _ = m.stage_times()
+        m.set_option(_lib.MOE_OPT_STAGE_TIMING, 0)
+        assert m.status() == 0, _lib.moe_error_string(m.status())
+        return max_over_ranks(ms, dist), stages
+
+    # routing statistics of the batches (for the algorithmic byte count)
     r = m.route(xp, Wg)
     counts_p = r["counts"].cpu().tolist()
+    idx_p = r["topk_idx"].cpu()
     r = m.route(xd, Wg)
     counts_d = r["counts"].cpu().tolist()
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         clk.wait_first()
-        ms_p, _ = timed(xp, args.steps, args.warmup, False, clk)
-        ms_pi, stages_p = timed(xp, max(args.steps // 2, 3), 0, True, clk)
-        ms_d, _ = timed(xd, args.decode_steps, args.warmup, False, clk)
-        ms_di, stages_d = timed(xd, max(args.decode_steps // 2, 3), 0, True, clk)
-    clocks = clk.summary()
+        # headline: K uninstrumented back-to-back calls after W warm-ups
+        ms_p, _ = timed(xp, yp, args.steps, args.warmup, False, clk, "headline")
+        # the same K calls again with per-kernel events: the kernels' shares of a call
+        ms_pi, stages_p = timed(xp, yp, args.steps, 0, True, clk, "prefill_stages")
+        ms_d, _ = timed_decode(args.decode_steps, False, clk, "decode")
+        ms_di, stages_d = timed_decode(max(args.decode_steps // 4, 3), True, clk, "decode_stages")
+        # sustained: a pre-roll into the power-capped steady state, then >= 2 s timed
+        sus = None
+        if args.sustained_s > 0:
+            n_sus = max(int(args.sustained_s / (ms_p * 1e-3)), args.steps)
+            n_pre = max(int(1.0 / (ms_p * 1e-3)), 1)
+            ms_s, _ = timed(xp, yp, n_sus, n_pre, False, clk, "sustained")
+            ms_si, stages_s = timed(xp, yp, max(n_sus // 3, args.steps), 0, True, clk, "sustained_stages")
+            sus = dict(ms=ms_s, calls=n_sus, ms_i=ms_si, stages=stages_s)
+    clocks = clk.summary(("headline",))
 
     # skewed, locally correlated routing at 32k context (router bias, repeated rows)
     skew = run_skewed(args, W1, W3, W2, pk, dist) if not args.no_skewed else None
@@ -271,21 +330,30 @@ def run_ours(args, rank, world, dist):
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)
 
     # decode with fp8 (e4m3) expert weights, power-of-two row scales
-    fp8 = run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist) if not args.no_fp8 else None
+    fp8 = run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist, flush) if not args.no_fp8 else None
 
     alg_p = algorithmic(wp.T, counts_p)
     alg_d = algorithmic(wd.T, counts_d)
     tok_s = world * wp.T / (ms_p * 1e-3)
-    # dominant kernel: the W1/W3 grouped GEMM (2/3 of the FLOPs)
-    k13_ms = stages_p.get("expert_w1w3_swiglu", float("nan"))
+    # dominant kernel: the W1/W3 grouped GEMM (2/3 of the FLOPs).  Its duration in
+    # the headline run = the headline's ms per call x its share of a call in the
+    # per-kernel events of the same calls repeated right after.
+    k13 = "expert_w1w3_swiglu"
+    share = stages_p[k13] / sum(stages_p.values())
+    k13_ms = ms_p * share
     achieved = alg_p["flops_w13"] / (k13_ms * 1e-3) / 1e12
     traffic, traffic_note = w13_traffic()
     roofline = {"kernel": "expert_w1w3_swiglu (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
-                "achieved": round(achieved, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
-                "peak_kind": f"bf16 sustained ({pk['source']})",
-                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4),
+                "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops"], 4),
+                "peak_kind": f"bf16 burst ({pk['source']}): the headline window is {args.steps} calls, "
+                             f"{ms_p * args.steps:.0f} ms",
+                "frac_of_nominal_2250": round(achieved / 2250.0, 4),
                 "flops_per_launch": alg_p["flops_w13"],
+                "duration_us": round(k13_ms * 1e3, 1),
+                "duration_source": "headline ms_per_step x the kernel's share of the per-kernel CUDA-event times "
+                                   "of the same calls repeated right after",
+                "share": round(share, 4), "instrumented_us": round(stages_p[k13] * 1e3, 1),
                 "traffic": traffic, "traffic_unit": "bytes per launch (dram read + write)",
                 "traffic_source": traffic_note}
     layer_tflops = alg_p["flops"] / (ms_p * 1e-3) / 1e12
@@ -296,14 +364,16 @@ def run_ours(args, rank, world, dist):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0, 1/sqrt(fan_in)) weights, unit-RMS x)",
         "config": {"workload": "prefill_t4096", "T": wp.T, "d": wp.d, "d_ff": wp.d_ff, "n_experts": wp.n_experts,
                    "k": wp.k, "parallelism": f"replicas x{world} (data parallel over tokens)",
-                   "l2": "inputs larger than L2: 2.82 GB of expert weights streamed per step"},
+                   "l2": "prefill: inputs larger than L2 (2.82 GB of expert weights streamed per step); "
+                         "decode: L2 overwritten (256 MB) before each timed call"},
         "layer": {"us_per_layer": round(ms_p * 1e3, 1), "tflops": round(layer_tflops, 1),
-                  "frac_of_bf16_sustained": round(layer_tflops / pk["bf16_tflops_sustained"], 4),
+                  "frac_of_bf16_burst": round(layer_tflops / pk["bf16_tflops"], 4),
                   "frac_of_bf16_nominal_2250": round(layer_tflops / 2250.0, 4), "expert_loads": counts_p},
         "decode_t32": {"us_per_layer": round(ms_d * 1e3, 1), "weight_gbytes": round(alg_d["weight_bytes"] / 1e9, 3),
                        "experts_touched": alg_d["touched"], "achieved_gbs": round(dec_gbs, 1),
                        "frac_of_hbm": round(dec_gbs / pk["hbm_gbs"], 4),
                        "frac_of_hbm_nominal_8000": round(dec_gbs / 8000.0, 4),
+                       "timing": "L2 overwritten before each call; CUDA events around each call",
                        "stages_us": {k: round(v * 1e3, 1) for k, v in stages_d.items()},
                        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"],
                                     "unit": "GB/s", "frac": round(dec_gbs / pk["hbm_gbs"], 4),
@@ -311,6 +381,7 @@ def run_ours(args, rank, world, dist):
         "stages_us": {k: round(v * 1e3, 1) for k, v in stages_p.items()},
         "instrumented_ms_per_step": {"prefill": round(ms_pi, 4), "decode": round(ms_di, 4)},
         "roofline": roofline,
+        "sustained": None,
         "skewed_t32768": skew,
         "decode_fp8": fp8,
         "e2e": {"value": round(world * wp.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
@@ -322,10 +393,27 @@ def run_ours(args, rank, world, dist):
                    "per_kernel": "CUDA events recorded by the library around each kernel on the call's stream"},
         "clocks": clocks,
     }
+    if sus is not None:
+        share_s = sus["stages"][k13] / sum(sus["stages"].values())
+        k13_s = sus["ms"] * share_s
+        ach_s = alg_p["flops_w13"] / (k13_s * 1e-3) / 1e12
+        lt = alg_p["flops"] / (sus["ms"] * 1e-3) / 1e12
+        line["sustained"] = {
+            "tokens_s": round(world * wp.T / (sus["ms"] * 1e-3), 1), "us_per_layer": round(sus["ms"] * 1e3, 1),
+            "calls": sus["calls"], "timed_seconds": round(sus["ms"] * sus["calls"] / 1e3, 2),
+            "layer_tflops": round(lt, 1), "layer_frac_of_nominal_2250": round(lt / 2250.0, 4),
+            "roofline": {"kernel": k13, "bound": "tensor", "achieved": round(ach_s, 1),
+                         "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": round(ach_s / pk["bf16_tflops_sustained"], 4),
+                         "peak_kind": f"bf16 sustained ({pk['source']})", "duration_us": round(k13_s * 1e3, 1),
+                         "share": round(share_s, 4)},
+            "stages_us": {k: round(v * 1e3, 1) for k, v in sus["stages"].items()},
+            "clocks": clk.summary(("sustained",)),
+            "note": "after a 1 s pre-roll of the same calls; per-kernel shares from the instrumented calls that follow"}
     m.close()
     host = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = dict(x=xp.cpu(), Wg=Wg.cpu(), W=(W1.cpu(), W3.cpu(), W2.cpu()))
+        host = dict(x=xp.cpu(), Wg=Wg.cpu(), W=(W1.cpu(), W3.cpu(), W2.cpu()), gpu_idx=idx_p)
     del xp, xd, W1, W3, W2, Wg
     torch.cuda.empty_cache()
     if not args.no_stack:
@@ -333,10 +421,11 @@ def run_ours(args, rank, world, dist):
     return line, host
 
 
-def run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist):
+def run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist, flush):
     """Decode batches through moe_forward_fp8: the same experts quantised to e4m3
     with one power-of-two scale per weight row (1.41 GB of weight bytes instead
-    of 2.82 GB), the same router.  Back-to-back calls, CUDA events."""
+    of 2.82 GB), the same router.  L2 overwritten before each call, CUDA events
+    around each call."""
     from sparse_mixture_experts_54_b300 import _lib, inputs
 
     q, s = {}, {}
@@ -345,7 +434,8 @@ def run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist):
     args8 = (q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     stream = torch.cuda.current_stream()
     w = inputs.workload("decode_t32")
-    out = {"weights": "e4m3, one fp32 power-of-two scale per weight row", "us_per_layer": {}}
+    out = {"weights": "e4m3, one fp32 power-of-two scale per weight row", "us_per_layer": {},
+           "timing": "L2 overwritten before each call; CUDA events around each call"}
 
     def timed(T, steps, stage_timing):
         x = inputs.make_x(w, "cuda", seed=17, T=T)
@@ -356,21 +446,16 @@ def run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist):
         m.set_option(_lib.MOE_OPT_STAGE_TIMING, 1 if stage_timing else 0)
         m.stage_times()
         barrier(dist)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            m.forward_fp8(x, Wg, *args8, y=y)
-        e1.record(stream)
-        torch.cuda.synchronize()
+        ms = timed_per_call(lambda: m.forward_fp8(x, Wg, *args8, y=y), steps, stream, flush)
         barrier(dist)
         stages, _ = m.stage_times()
         m.set_option(_lib.MOE_OPT_STAGE_TIMING, 0)
         assert m.status() == 0, _lib.moe_error_string(m.status())
         counts = m.route(x, Wg)["counts"].cpu().tolist()
-        return max_over_ranks(e0.elapsed_time(e1) / steps, dist), stages, counts
+        return max_over_ranks(ms, dist), stages, counts
 
     ms, _, counts = timed(32, args.decode_steps, False)
-    _, stages, _ = timed(32, max(args.decode_steps // 2, 3), True)
+    _, stages, _ = timed(32, max(args.decode_steps // 4, 3), True)
     touched = sum(1 for c in counts if c > 0)
     wbytes = touched * (3 * w.d * w.d_ff + (2 * w.d_ff + w.d) * 4)   # e4m3 bytes + row scales
     nbytes = wbytes + 2 * 32 * w.d * 2 + w.n_experts * w.d * 4
@@ -518,6 +603,27 @@ def time_oracle(x, Wg, W, budget_s: float, min_tokens: int, seed: int = 0):
     return dict(tokens=done, seconds=t_total, threads=threads, tok_s=done / t_total)
 
 
+def routing_near_ties(host, K: int = 2, eps: float = 1e-6):
+    """The cpu_baseline leg's fp64 routing of every prefill token against the GPU's
+    top-K indices: near ties (fp64 logits of ranks 1..K+1 closer than eps, where
+    fp32 on the GPU may order them either way) and index mismatches outside them."""
+    import numpy as np
+
+    import oracle
+    from sparse_mixture_experts_54_b300 import inputs
+
+    logits = oracle.router_logits(inputs.to_oracle(host["x"]), inputs.to_oracle(host["Wg"]))
+    idx, _ = oracle.select_topk(logits, K)
+    srt = -np.sort(-logits, axis=1)
+    gaps = srt[:, :K] - srt[:, 1:K + 1]
+    near = np.any(gaps < eps, axis=1)
+    gpu = host["gpu_idx"].numpy()
+    mism = int(np.sum(np.any(gpu != idx, axis=1) & ~near))
+    return {"tokens": int(logits.shape[0]), "near_ties": int(near.sum()), "index_mismatches_outside_near_ties": mism,
+            "rule": f"fp64 router logits of ranks 1..{K + 1} closer than {eps:g}",
+            "source": "cpu_baseline leg: the oracle's fp64 routing of every token vs the GPU's top-k"}
+
+
 def cpu_baseline_block(res, T):
     return {"value": round(res["tok_s"], 3), "unit": "tokens/s", "cores": res["threads"], "kind": "oracle",
             "sample": f"{res['tokens']} of the {T} prefill tokens (seeded sample), full routing + 2 SwiGLU experts "
@@ -550,6 +656,8 @@ def run_reference(args, rank, world):
                                  seconds=sum(r["seconds"] for r in per_step)), w.T)
     return {"impl": "reference", "metric": METRIC, "value": round(tok_s, 3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 1),
+            "ms_per_step_kind": "extrapolated: T=4096 tokens divided by the oracle's rate on the timed samples "
+                                "(each step times a bounded sample, not the whole batch)",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0, 1/sqrt(fan_in)) weights, unit-RMS x)",
             "config": {"workload": "prefill_t4096", "T": w.T, "d": w.d, "d_ff": w.d_ff, "n_experts": w.n_experts,
@@ -598,6 +706,8 @@ def main():
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8-weight decode measurements")
     ap.add_argument("--fp8", action="store_true", help="with --profile-step: fp8 expert weights (moe_forward_fp8)")
     ap.add_argument("--stack-passes", type=int, default=8)
+    ap.add_argument("--sustained-s", type=float, default=2.5,
+                    help="seconds of back-to-back prefill calls for the sustained leg (0: skip it)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=None,
                     help="oracle seconds per reference step (default: min(6, 150 / (warmup + steps)))")
@@ -621,6 +731,7 @@ def main():
         if host is not None:
             res = time_oracle(host["x"], host["Wg"], host["W"], budget_s=args.cpu_budget_s, min_tokens=8)
             line["cpu_baseline"] = cpu_baseline_block(res, 4096)
+            line["near_ties"] = routing_near_ties(host)
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)

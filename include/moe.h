@@ -29,9 +29,14 @@
  *    stream; the library never frees caller memory.
  *  - All compute entry points are asynchronous on `stream` and do not
  *    synchronise the host.  Argument errors are returned synchronously
- *    (moe_status_t).  Failures inside kernels (a bounded wait that ran out, a
- *    failed debug bounds check) are recorded in a sticky status word that
+ *    (moe_status_t).  Failures inside kernels (a bounded wait that ran out, an
+ *    index check of the routing and dispatch kernels that failed: an expert id
+ *    outside [0, n) or a dispatch position outside [0, k*T), which is then
+ *    never used as an address) are recorded in a sticky status word that
  *    moe_status() reads without synchronising.
+ *  - Each forward call is one NVTX range on the calling host thread ("moe_forward"
+ *    or "moe_forward_fp8") holding one nested range per stage, named as the
+ *    stages of moe_stage_times; a profiler that records NVTX shows them.
  *  - A context must not be used from two host threads at once; calls on
  *    different streams with the same context share its workspace and must be
  *    ordered by the caller.
@@ -267,7 +272,10 @@ const char* moe_stage_name(int i);
  *    layers in flight) race on it: order them on one stream.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The cached address belongs to the
+ *    device's primary context as it was then: after cudaDeviceReset (or any
+ *    other teardown of that context) it is stale, so this entry point must not
+ *    be used across a device reset.
  *  - Arguments: as moe_forward, plus the shape (d, d_ff, n_experts, k), the
  *    element type (moe_dtype_t) and an optional router bias b_g [n] (device,
  *    fp32, NULL for none).  status, if not NULL, is a caller-owned device int

@@ -6,6 +6,8 @@
 #include <array>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe.h"
 #include "kernels.h"
 
@@ -225,13 +227,20 @@ bool use_pair2(const moe_ctx* c) { return c->gemm_pair != 1 && pair_gemm_availab
 constexpr int kStages = 4;
 const char* const kStageNames[kStages] = {"route", "expert_w1w3_swiglu", "expert_w2_gate", "combine"};
 
-// Events of the current call when stage timing is on (null otherwise).
+// Stage boundaries of the current call: an NVTX range per stage on the host
+// thread that launches it (named as the stages of moe_stage_times, nested in
+// one range for the call), and CUDA events on the call's stream when stage
+// timing is on.
 struct StageMarks {
     moe_ctx* c = nullptr;
     cudaStream_t s = nullptr;
     std::array<cudaEvent_t, 5> ev{};
     bool on = false;
-    StageMarks(moe_ctx* ctx, cudaStream_t st) : c(ctx), s(st) {
+    int nvtx_depth = 0;
+    StageMarks(moe_ctx* ctx, cudaStream_t st, const char* call = "moe_forward") : c(ctx), s(st) {
+        nvtxRangePushA(call);
+        nvtxRangePushA(kStageNames[0]);
+        nvtx_depth = 2;
         if (!c->stage_timing) return;
         for (int i = 0; i <= kStages; ++i) {
             if (!c->ev_free.empty()) {
@@ -246,6 +255,14 @@ struct StageMarks {
         cudaEventRecord(ev[0], s);
     }
     void mark(int stage) {
+        if (nvtx_depth == 2) {
+            nvtxRangePop();
+            if (stage + 1 < kStages) {
+                nvtxRangePushA(kStageNames[stage + 1]);
+            } else {
+                nvtx_depth = 1;
+            }
+        }
         if (on) cudaEventRecord(ev[stage + 1], s);
     }
     void finish() {
@@ -255,6 +272,7 @@ struct StageMarks {
         }
     }
     ~StageMarks() {
+        while (nvtx_depth-- > 0) nvtxRangePop();
         if (on)
             for (int i = 0; i <= kStages; ++i) c->ev_free.push_back(ev[i]);
     }
@@ -366,7 +384,7 @@ int run_forward_fp8(moe_ctx* c, const void* x, const float* Wg, const uint8_t* W
                     const uint8_t* W3q, const float* W3s, const uint8_t* W2q, const float* W2s, void* y, int T,
                     cudaStream_t s) {
     const int R = c->k * T;
-    StageMarks marks(c, s);
+    StageMarks marks(c, s, "moe_forward_fp8");
     int rc = run_route(c, x, Wg, T, s, nullptr, true);
     if (rc != MOE_OK) return rc;
     marks.mark(0);

@@ -457,9 +457,15 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     const unsigned lt_mask = (1u << lane) - 1u;
     const uint4* xv4 = static_cast<const uint4*>(p.x);
     uint4* xp4 = static_cast<uint4*>(p.Xp);
+    const int R = p.T * K;
     for (int a0 = a_begin; a0 < a_end; a0 += FR_ROUND) {
         const int a = a0 + tid;
-        const int e = a < a_end ? p.topk_idx[a] : -1;   // this block's own phase-1 writes
+        int e = a < a_end ? p.topk_idx[a] : -1;   // this block's own phase-1 writes
+        // Index checks on every placement (one compare each): an expert id
+        // outside [0, n) or a position outside [0, K*T) is never used as an
+        // address; the call records MOE_ERR_BOUNDS in the status word instead.
+        bool bad = a < a_end && (e < 0 || e >= n);
+        if (bad) e = -1;
         wtab[warp][lane] = 0;
         __syncwarp();
         const unsigned same = __match_any_sync(0xffffffffu, e);
@@ -483,9 +489,17 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
         __syncthreads();
         if (e >= 0) {
             const int pos = s_base[e] + wtab[warp][e] + rank;
-            p.perm[pos] = a;
-            p.inv[a] = pos;
-            placed[tid] = make_int2(a, pos);
+            if (pos >= 0 && pos < R) {
+                p.perm[pos] = a;
+                p.inv[a] = pos;
+                placed[tid] = make_int2(a, pos);
+            } else {
+                bad = true;
+            }
+        }
+        if (bad) {
+            placed[tid] = make_int2(a, -1);
+            report(p.st, kStatusBounds);
         }
         __syncthreads();
         if (xp4) {
@@ -495,6 +509,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
             // (a whole 8 KB bf16 row of the Mixtral shape)
             for (int r = warp; r < nr; r += FR_WARPS) {
                 const int2 ap = placed[r];
+                if (ap.y < 0) continue;
                 const int t = ap.x / K;
                 const uint4* src = xv4 + static_cast<size_t>(t) * rv;
                 uint4* dst = xp4 + static_cast<size_t>(ap.y) * rv;

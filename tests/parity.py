@@ -95,3 +95,46 @@ def y_to_numpy(y: torch.Tensor) -> np.ndarray:
 
 def oracle_args(layer: dict):
     return tuple(inputs.to_oracle(layer[k]) for k in ("x", "Wg", "W1", "W3", "W2")) + (inputs.to_oracle(layer["bias"]),)
+
+
+# Row boundaries inside a 256-row block of one expert's rows that the tiled
+# kernels treat differently: 32-row epilogue quadrants, the 64-row halves of a
+# CTA pair's 128-row tail tile, 128-row single-CTA tiles and the two CTAs of a
+# 256-row pair tile.
+EDGE_ROWS_FINE = (0, 31, 32, 63, 64, 95, 96, 127, 128, 255)
+EDGE_ROWS = (0, 127, 128, 255)
+
+
+def dispatch_sample(counts, offsets, perm, K: int, T: int, n_random: int, seed: int = 0,
+                    edges=EDGE_ROWS_FINE):
+    """Tokens for a sampled check at full size, picked from the GPU's own
+    expert-contiguous order (which check_dispatch has already compared with the
+    oracle's), so that every tiling boundary of every expert is covered:
+
+    * n_random seeded tokens;
+    * every token of the smallest non-empty expert group;
+    * the tokens at the ``edges`` rows of every 256-row block of every expert;
+    * every row of each expert's last 128-row tile (its ragged tail, including
+      the most loaded expert's).
+
+    Returns (sorted token numbers, dict of how many rows each rule picked)."""
+    counts = np.asarray(counts, dtype=np.int64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    perm = np.asarray(perm, dtype=np.int64)
+    rows_edge, rows_tail, rows_small = [], [], []
+    for e in range(counts.size):
+        c, o = int(counts[e]), int(offsets[e])
+        if c == 0:
+            continue
+        for b in range(0, c, 256):
+            rows_edge += [o + b + r for r in edges if b + r < c]
+        last = (c - 1) // 128 * 128
+        rows_tail += list(range(o + last, o + c))
+    nz = np.nonzero(counts)[0]
+    small = int(nz[np.argmin(counts[nz])])
+    rows_small = list(range(int(offsets[small]), int(offsets[small] + counts[small])))
+    rows = np.asarray(sorted(set(rows_edge) | set(rows_tail) | set(rows_small)), dtype=np.int64)
+    toks = set((perm[rows] // K).tolist()) | set(inputs.sample_tokens(T, n_random, seed).tolist())
+    info = dict(random=min(n_random, T), edge_rows=len(set(rows_edge)), tail_rows=len(set(rows_tail)),
+                smallest_expert=small, smallest_rows=len(rows_small))
+    return np.asarray(sorted(toks), dtype=np.int64), info

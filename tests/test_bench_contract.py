@@ -67,3 +67,26 @@ def test_e2e_cpu_baseline_and_clocks(line):
     for key in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert key in k, key
     assert not set(k["reasons"]) & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def test_roofline_duration_comes_from_the_headline_run(line):
+    # the W1/W3 duration is the headline's ms per call times the kernel's share of
+    # the per-kernel event times, and the peak is the burst one for that window
+    r = line["roofline"]
+    assert r["duration_us"] == pytest.approx(line["ms_per_step"] * 1e3 * r["share"], rel=2e-3)
+    assert r["achieved"] == pytest.approx(r["flops_per_launch"] / (r["duration_us"] * 1e-6) / 1e12, rel=2e-3)
+    assert "burst" in r["peak_kind"]
+    share = line["stages_us"]["expert_w1w3_swiglu"] / sum(line["stages_us"].values())
+    assert r["share"] == pytest.approx(share, abs=2e-3)
+
+
+def test_sustained_leg_and_near_ties(line):
+    s = line["sustained"]
+    assert s["timed_seconds"] >= 2.0
+    r = s["roofline"]
+    assert "sustained" in r["peak_kind"] and r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-3)
+    assert s["clocks"]["samples"] >= 5
+    assert not set(s["clocks"]["reasons"]) & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    nt = line["near_ties"]
+    assert nt["tokens"] == line["config"]["T"]
+    assert nt["index_mismatches_outside_near_ties"] == 0

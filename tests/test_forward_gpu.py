@@ -4,7 +4,8 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_close, check_route, near_tie_mask, reference_selection, y_to_numpy
+from parity import (EDGE_ROWS, EDGE_ROWS_FINE, assert_close, check_dispatch, check_route, dispatch_sample,
+                    reference_selection, y_to_numpy)
 from sparse_mixture_experts_54_b300 import _lib, inputs
 from sparse_mixture_experts_54_b300.layer import MoELayer
 
@@ -214,6 +215,10 @@ def test_forward_replays_from_a_cuda_graph(T):
 
 
 # ----------------------------------------------------------------------------- Mixtral shape
+# d = 4096, d_ff = 14336, 8 experts, top-2 (xyznot "Method"; aiqianji 2.1.2), with
+# the seeded weight and token distributions of the workloads.  The oracle's fp64
+# routing covers every token; its expert outputs cover the tokens each case
+# lists.  One oracle result serves every kernel configuration of a case.
 @pytest.fixture(scope="module")
 def mixtral_experts():
     w = inputs.workload("decode_t32")
@@ -222,39 +227,92 @@ def mixtral_experts():
     return (W1, W3, W2), host
 
 
-def _mixtral_case(name, mixtral_experts, sample, path=0, pair=0):
-    w = inputs.workload(name)
-    (W1, W3, W2), (h1, h3, h2) = mixtral_experts
-    x = inputs.make_x(w, "cuda")
-    Wg, b = inputs.make_router(w, "cuda")
-    layer = dict(x=x, Wg=Wg, bias=b, W1=W1, W3=W3, W2=W2)
-    m, y, gidx, gw = run_layer(w, layer, path, pair)
-    toks = inputs.sample_tokens(w.T, sample).numpy()
-    xo, Wgo, bo = inputs.to_oracle(x), inputs.to_oracle(Wg), inputs.to_oracle(b)
-    logits = oracle.router_logits(xo, Wgo, bo)
-    idx, gate = oracle.select_topk(logits, w.k)
-    near = check_route(gidx, gw, logits, idx, gate, w.k)
-    idx_u, gate_u, _ = reference_selection(dict(logits=logits, idx=idx, gate=gate), gidx, w.k)
-    y_ref = oracle.moe_tokens(xo, h1, h3, h2, idx_u, gate_u, toks)
-    err, bound = assert_close(y_to_numpy(y)[toks], y_ref, "bf16")
-    print(f"{name}: {len(toks)} tokens checked, max err {err:.3e} (bound {bound:.3e}), near ties {near}")
-    m.close()
+class MixtralCase:
+    """One Mixtral-shape batch: the GPU's routing and dispatch checked against the
+    oracle (indices bit-exact except near ties, dispatch bit-exact on the GPU's
+    own indices), the tokens to check and the oracle's outputs for them."""
+
+    def __init__(self, name, experts, T=None, seed=None, n_random=None, edges=EDGE_ROWS_FINE):
+        w = inputs.workload(name) if T is None else inputs.workload(name, T=T)
+        (self.W1, self.W3, self.W2), (h1, h3, h2) = experts
+        self.w = w
+        self.x = inputs.make_x(w, "cuda", seed=seed)
+        self.Wg, self.b = inputs.make_router(w, "cuda")
+        m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=self.b)
+        r = m.route(self.x, self.Wg)
+        torch.cuda.synchronize()
+        gidx, gw = r["topk_idx"].cpu().numpy(), r["topk_w"].cpu().numpy()
+        counts, offsets, perm = (r[k].cpu().numpy() for k in ("counts", "offsets", "perm"))
+        m.close()
+        xo, Wgo, bo = inputs.to_oracle(self.x), inputs.to_oracle(self.Wg), inputs.to_oracle(self.b)
+        logits = oracle.router_logits(xo, Wgo, bo)
+        idx, gate = oracle.select_topk(logits, w.k)
+        self.near = check_route(gidx, gw, logits, idx, gate, w.k)
+        check_dispatch(gidx, counts, offsets, perm, w.n_experts)
+        if n_random is None:
+            self.toks, self.info = np.arange(w.T), dict(all_tokens=w.T)
+        else:
+            self.toks, self.info = dispatch_sample(counts, offsets, perm, w.k, w.T, n_random, edges=edges)
+        self.counts = counts.tolist()
+        idx_u, gate_u, _ = reference_selection(dict(logits=logits, idx=idx, gate=gate), gidx, w.k)
+        self.y_ref = oracle.moe_tokens(xo, h1, h3, h2, idx_u, gate_u, self.toks)
+
+    def check(self, path=0, pair=0):
+        w = self.w
+        layer = dict(x=self.x, Wg=self.Wg, bias=self.b, W1=self.W1, W3=self.W3, W2=self.W2)
+        m, y, gidx, _ = run_layer(w, layer, path, pair)
+        m.close()
+        err, bound = assert_close(y_to_numpy(y)[self.toks], self.y_ref, "bf16")
+        print(f"{w.name} T={w.T} path={path} pair={pair}: {len(self.toks)} tokens checked {self.info}, "
+              f"loads {self.counts}, max err {err:.3e} (bound {bound:.3e}), near ties {self.near}")
+        return err
 
 
-def test_mixtral_decode_t32_full(mixtral_experts):
-    _mixtral_case("decode_t32", mixtral_experts, 32)
+@pytest.fixture(scope="module")
+def prefill_case(mixtral_experts):
+    # 512 seeded tokens + the smallest expert group + every tile edge and tail
+    return MixtralCase("prefill_t4096", mixtral_experts, n_random=512)
 
 
-def test_mixtral_prefill_t4096_sampled(mixtral_experts):
-    _mixtral_case("prefill_t4096", mixtral_experts, 48)
+@pytest.fixture(scope="module")
+def skewed_case(mixtral_experts):
+    return MixtralCase("skewed_t32768", mixtral_experts, n_random=512, edges=EDGE_ROWS)
 
 
-def test_mixtral_prefill_t4096_single_cta(mixtral_experts):
-    _mixtral_case("prefill_t4096", mixtral_experts, 48, pair=1)
+@pytest.mark.parametrize("pair", [0, 1, 2], ids=["default", "single_cta", "cta_pairs"])
+def test_mixtral_prefill_t4096(prefill_case, pair):
+    prefill_case.check(pair=pair)
 
 
-def test_mixtral_skewed_t32768_sampled(mixtral_experts):
-    _mixtral_case("skewed_t32768", mixtral_experts, 48)
+@pytest.mark.parametrize("pair", [0, 1, 2], ids=["default", "single_cta", "cta_pairs"])
+def test_mixtral_skewed_t32768(skewed_case, pair):
+    case = skewed_case
+    assert max(case.counts) > 0.3 * sum(case.counts)   # the hot expert takes > 30% of the rows
+    case.check(pair=pair)
+
+
+_DECODE_CASES = {}
+
+
+@pytest.fixture(scope="module")
+def decode_cases(mixtral_experts):
+    """Mixtral-shape decode batches, every token checked, built on first use."""
+    def get(T):
+        if T not in _DECODE_CASES:
+            _DECODE_CASES[T] = MixtralCase("decode_t32", mixtral_experts, T=T, seed=None if T == 32 else 40 + T)
+        return _DECODE_CASES[T]
+    yield get
+    _DECODE_CASES.clear()
+
+
+# (T, forced path): 0 = the default for that T (weight streaming up to T = 128,
+# grouped GEMMs above), 1 = grouped GEMMs, 2 = weight streaming
+MIXTRAL_DECODE = [(1, 0), (32, 0), (32, 1), (128, 0), (128, 1), (256, 0), (256, 2)]
+
+
+@pytest.mark.parametrize("T,path", MIXTRAL_DECODE, ids=[f"T{T}-path{p}" for T, p in MIXTRAL_DECODE])
+def test_mixtral_decode_sweep(decode_cases, T, path):
+    decode_cases(T).check(path=path)
 
 
 # ----------------------------------------------------------------------------- decode (weight-streaming) path
@@ -301,7 +359,3 @@ def test_decode_and_grouped_paths_agree_and_are_deterministic():
     _, y_grp, _, _ = run_layer(w, layer, path=1)
     assert torch.equal(y_dec, y_dec2)
     assert_close(y_to_numpy(y_dec), y_to_numpy(y_grp), "bf16")
-
-
-def test_mixtral_decode_t32_grouped_path(mixtral_experts):
-    _mixtral_case("decode_t32", mixtral_experts, 32, path=1)

@@ -210,45 +210,71 @@ def bits_to_device(bits):
 @pytest.mark.slow
 def test_mixtral_stack32_every_layer_from_the_oracle_state(mixtral_stack):
     """Each of the 32 layers at the Mixtral shape, started from the oracle's own
-    state: the oracle carries 8 decode rows and 4 sampled rows of a T=8192 prefill
-    batch through the stack in fp64/bf16; before each layer those rows are copied
-    into the GPU's batches (the prefill batch's other rows follow the GPU's own
-    path -- rows do not interact), the GPU runs the block, and its rows must match
-    the oracle's next state within the single-layer bound.  Two independent bf16
-    trajectories drift apart by ~1% of rms(h) within ten layers, so near ties
-    make a whole-stack comparison of the two paths meaningless at this depth."""
+    state, for every batch size of the stack workload's sweep: the oracle carries
+    a few rows of each batch (all 8 rows of T=8, the single row of T=1, 4
+    sampled rows of T=128, of T=256 and of the T=8192 prefill batch) through the
+    stack in fp64/bf16; before each layer those rows are copied into the GPU's
+    batches (the batches' other rows follow the GPU's own path -- rows do not
+    interact), the GPU runs the block, and its rows must match the oracle's next
+    state within the single-layer bound.  T=256 runs twice, on the default path
+    (grouped GEMMs) and forced onto weight streaming; T <= 128 runs weight
+    streaming by default.  Two independent bf16 trajectories drift apart by ~1%
+    of rms(h) within ten layers, so near ties make a whole-stack comparison of
+    the two paths meaningless at this depth."""
     w, layers = mixtral_stack
-    T_dec, T_pre, n_pre = 8, inputs.STACK_PREFILL_T, 4
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
-    m.reserve(T_pre)
-    hp = inputs.make_x(w, "cuda", seed=2001, T=T_pre)
-    toks = inputs.sample_tokens(T_pre, n_pre, seed=3).numpy()
-    toks_d = torch.from_numpy(toks).cuda()
-    rows = np.concatenate([inputs.to_oracle(inputs.make_x(w, "cuda", seed=2000, T=T_dec)),
-                           inputs.to_oracle(hp)[toks]], axis=0)
-    errs, near_total = [], 0
+    m.reserve(inputs.STACK_PREFILL_T)
+    m_dec = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
+    m_dec.set_option(_lib.MOE_OPT_FORCE_PATH, 2)
+    # (name, T, sampled rows or None for all, context, seed of h0); a batch whose
+    # name repeats an earlier one shares that batch's oracle rows
+    spec = [("decode_t8", 8, None, m, 2000), ("decode_t1", 1, None, m, 2002),
+            ("decode_t128", 128, 4, m, 2003), ("decode_t256", 256, 4, m, 2004),
+            ("decode_t256", 256, 4, m_dec, 2004), ("prefill_t8192", inputs.STACK_PREFILL_T, 4, m, 2001)]
+    batches, rows, seg, names = [], [], {}, []
+    for i, (name, T, ns, ctx, seed) in enumerate(spec):
+        h = inputs.make_x(w, "cuda", seed=seed, T=T)
+        toks = np.arange(T) if ns is None else inputs.sample_tokens(T, ns, seed=3 + i).numpy()
+        if name not in seg:
+            start = sum(len(r) for r in rows)
+            rows.append(inputs.to_oracle(h)[toks])
+            seg[name] = (start, start + len(toks))
+            names.append(name)
+        batches.append((name, h, torch.from_numpy(toks).cuda(), ctx))
+    rows = np.concatenate(rows, axis=0)
+    n_rows = rows.shape[0]
+    errs, near_total = {n: [] for n in names}, 0
     for l, lw in enumerate(layers):
         ref = oracle.block_forward(rows, *(inputs.to_oracle(t) for t in lw), w.k, EPS)
-        hd = bits_to_device(rows[:T_dec])
-        hp[toks_d] = bits_to_device(rows[T_dec:])
-        m.block_forward(hd, *lw, EPS)
-        m.block_forward(hp, *lw, EPS)
+        for name, h, toks_d, ctx in batches:
+            a, b = seg[name]
+            h[toks_d] = bits_to_device(rows[a:b])
+            ctx.block_forward(h, *lw, EPS)
         torch.cuda.synchronize()
-        assert m.status() == 0, f"layer {l}: {_lib.moe_error_string(m.status())}"
-        got = torch.cat([hd, hp[toks_d]], dim=0).float().cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(got))
+        assert m.status() == 0 and m_dec.status() == 0, f"layer {l}: {_lib.moe_error_string(m.status())}"
         near = near_tie_mask(ref["logits"], w.k, 1e-3)
         near_total += int(near.sum())
         y_rms = np.sqrt(np.mean(ref["y"] ** 2, axis=1, keepdims=True))
         allowed = BF16_STORE * np.abs(ref["h_new"]) + BF16_TOL * y_rms
-        diff = np.abs(got - ref["h_new"])
-        excess = (diff - allowed)[~near]
-        assert excess.size == 0 or excess.max() <= 0.0, \
-            f"layer {l}: error beyond the bound by {excess.max():.3e} (raw max {diff[~near].max():.3e})"
-        errs.append(float((diff - BF16_STORE * np.abs(ref["h_new"]))[~near].max() / y_rms.max()))
+        for bi, (name, h, toks_d, ctx) in enumerate(batches):
+            a, b = seg[name]
+            got = h[toks_d].float().cpu().numpy().astype(np.float64)
+            assert np.all(np.isfinite(got)), f"layer {l} batch {bi} ({name}): non-finite"
+            diff = np.abs(got - ref["h_new"][a:b])
+            keep = ~near[a:b]
+            excess = (diff - allowed[a:b])[keep]
+            assert excess.size == 0 or excess.max() <= 0.0, \
+                f"layer {l} batch {bi} ({name}): error beyond the bound by {excess.max():.3e} " \
+                f"(raw max {diff[keep].max():.3e})"
+            if keep.any():
+                errs[name].append(float((diff - BF16_STORE * np.abs(ref["h_new"][a:b]))[keep].max()
+                                        / y_rms[a:b].max()))
         rows = ref["h_bits"]
-    print(f"stack32 from the oracle state: max error beyond storage rounding, per layer, in units of "
-          f"rms(y): max {max(errs):.2e}, mean {np.mean(errs):.2e}; near-tie rows {near_total} of {12 * len(layers)}")
+    summary = {n: f"{max(e):.2e}" for n, e in errs.items() if e}
+    print(f"stack32 from the oracle state: max error beyond storage rounding over the layers, in units of "
+          f"rms(y), per batch {summary}; near-tie rows {near_total} of {n_rows * len(layers)}")
+    m.close()
+    m_dec.close()
 
 
 @pytest.mark.slow
