@@ -471,6 +471,12 @@ def run_fp8_decode(args, m, W1, W3, W2, Wg, pk, dist, flush):
         ms_t, _, _ = timed(T, max(args.decode_steps // 4, 20), False)
         out["us_per_layer"][str(T)] = round(ms_t * 1e3, 1)
     out["us_per_layer"]["32"] = round(ms * 1e3, 1)
+    out["kernel"] = "e4m3 weights into the 8-bit MMA against hi/lo e4m3 token rows (MOE_OPT_FP8_WIDEN 0)"
+    # the exact widening kernel beside it (bitwise equal to the bf16 path on the dequantised weights)
+    m.set_option(_lib.MOE_OPT_FP8_WIDEN, 1)
+    ms_w, stages_w, _ = timed(32, max(args.decode_steps // 4, 20), False)
+    m.set_option(_lib.MOE_OPT_FP8_WIDEN, 0)
+    out["widened_t32_us_per_layer"] = round(ms_w * 1e3, 1)
     del q, s, args8
     torch.cuda.empty_cache()
     return out

@@ -11,7 +11,10 @@
 // bf16 (after adding the residual row h, when given) and writes y, then puts
 // the counter back to 0 for the next call.  The
 // sum and its order are the same whichever row arrives last, so y is bitwise
-// reproducible.
+// reproducible.  Once the sum is written, the K slot-row segments are dead
+// (nothing reads them again in this call, and the next call writes them before
+// reading): the warp drops their L2 lines without writing them back to DRAM
+// (discard.global.L2), so rows that are still in L2 never reach DRAM.
 #pragma once
 
 #include "common.cuh"
@@ -28,6 +31,11 @@ struct CombineArgs {
 };
 
 __device__ __forceinline__ float4 ldcg_f4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// Invalidate the 128-byte L2 line at p (128-byte aligned) without writing it back.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
 
 // Called by all 32 lanes of an epilogue warp after each lane has written its
 // row's features [128 blk, 128 blk + 128) of Ys (row = flat assignment a,
@@ -99,6 +107,14 @@ __device__ __forceinline__ void combine_arrive(const CombineArgs& c, const float
                 *reinterpret_cast<uint2*>(c.y + static_cast<size_t>(tt[r]) * c.d + col) = o;
                 if (lane == 0) c.cnt[static_cast<size_t>(tt[r]) * c.nblk + blk] = 0;
             }
+        }
+        // every lane's loads of the slot rows have been consumed above; lanes 0, 8,
+        // 16 and 24 each drop one of the four 128-byte lines of a row's 512-byte segment
+        __syncwarp();
+        if ((lane & 7) == 0) {
+            for (int r = 0; r < nr; ++r)
+                for (int k = 0; k < c.K; ++k)
+                    discard_l2_line(Ys + (static_cast<size_t>(tt[r]) * c.K + k) * ldY + blk * 128 + (lane >> 3) * 32);
         }
     }
 }

@@ -101,6 +101,32 @@ cudaError_t launch_pair_gemm2(const CUtensorMap& mapH, const CUtensorMap& mapW2_
 // weight-streaming decode path (bf16, small T) ----------------------------------
 constexpr int kDecodeMaxT = 256;     // tokens per call the decode kernels accept
 constexpr int kDecodeMaxSplits = 16;
+
+// Sum of the S (<= kDecodeMaxSplits) K-split partials p[s * stride], added in
+// s order.  The loads are issued eight at a time before their adds, so a small
+// batch's few threads wait for S/8 round trips to L2 instead of S in a row.
+__device__ __forceinline__ float4 sum_splits(const float4* __restrict__ p, size_t stride, int S) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < S) v[j] = __ldg(p + static_cast<size_t>(s0 + j) * stride);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j == 0) {
+                a = v[0];
+            } else if (s0 + j < S) {
+                a.x += v[j].x;
+                a.y += v[j].y;
+                a.z += v[j].z;
+                a.w += v[j].w;
+            }
+        }
+    }
+    return a;
+}
+
 int decode_pick_splits(int units, int kblocks, int num_sms);
 cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
                               const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,
@@ -112,6 +138,44 @@ cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R,
 cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
                                   int T, int K, int d, const void* resid, void* y, cudaStream_t s);
 
+// the whole small-batch layer in one cooperative persistent kernel
+// (decode_fused.cu): routing, dispatch, gather, W1/W3 and W2 weight streaming,
+// SwiGLU and combine, with grid-wide barriers between the steps.  bar holds
+// fused_decode_bar_ints() ints that must be zero before the first call; every
+// complete call leaves them as it found them.  rstd non-null: RMSNorm the rows
+// first (the residual block; resid then is the residual, usually x == y).
+struct FusedDecodeInput {
+    const __nv_bfloat16* x;
+    const float* Wg;
+    const float* bias;
+    const __nv_bfloat16* resid;
+    __nv_bfloat16* y;
+    int T, d, F, n, K;
+    float norm_eps;
+    int32_t* topk_idx;
+    float* topk_w;
+    float* rstd;
+    int* sched;
+    int32_t* perm;
+    int32_t* inv;
+    __nv_bfloat16* Xp;
+    __nv_bfloat16* H;
+    float* Pa;
+    float* Pb;
+    float* P2;
+    int* bar;
+    KStatus st;
+};
+int fused_decode_bar_ints();
+bool fused_decode_supported(int T, int d, int F, int n, int K, int num_sms);
+// Sets the kernel's shared-memory limit and checks that one CTA per SM fits
+// (cudaErrorNotSupported otherwise); no launch.
+cudaError_t prepare_decode_fused(const FusedDecodeInput& in, int num_sms);
+// mW1/mW3/mW2: 128-row boxes of the weights; mXp32/mH32: 32-row boxes of Xp and H
+cudaError_t launch_decode_fused(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUtensorMap& mW2,
+                                const CUtensorMap& mXp32, const CUtensorMap& mH32, const FusedDecodeInput& in,
+                                int num_sms, cudaStream_t s);
+
 // the same with e4m3 weights and fp32 row scales (decode_fp8.cu); the weight
 // maps come from encode_map_u8_sw64, the partial sums feed launch_decode_swiglu /
 // launch_decode_combine unchanged
@@ -122,6 +186,23 @@ cudaError_t launch_decode_fp8_w13(const CUtensorMap& mapW1q, const CUtensorMap& 
 cudaError_t launch_decode_fp8_w2(const CUtensorMap& mapW2q, const CUtensorMap& mapH32, const float* W2s,
                                  const int* sched, int n, int d, int F, int T, int K, int splits, float* P2, KStatus st,
                                  int num_sms, cudaStream_t s);
+
+// the same with e4m3 weights multiplied by the e4m3 tensor-core MMA
+// (decode_fp8_mma.cu): token rows split into hi/lo e4m3 rows with a
+// power-of-two scale per row; weight maps from encode_map_u8_sw128 (128-row
+// boxes), token maps with 64-row boxes; partial sums as above
+bool encode_map_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+cudaError_t launch_split_rows_e4m3(const __nv_bfloat16* X, int R, int d, uint8_t* Xq, float* xinv, cudaStream_t s);
+// chunks: the W2 GEMM's K splits (one H scale per row and split); hinv [chunks][R]
+cudaError_t launch_decode_swiglu_split(const float* Pa, const float* Pb, int S, int R, int F, int chunks, uint8_t* Hq,
+                                       float* hinv, cudaStream_t s);
+cudaError_t launch_decode_f8_w13(const CUtensorMap& mapW1q, const CUtensorMap& mapW3q, const CUtensorMap& mapXq,
+                                 const float* W1s, const float* W3s, const float* xinv, const int* sched, int n, int d,
+                                 int F, int T, int K, int splits, float* Pa, float* Pb, KStatus st, int num_sms,
+                                 cudaStream_t s);
+cudaError_t launch_decode_f8_w2(const CUtensorMap& mapW2q, const CUtensorMap& mapHq, const float* W2s,
+                                const float* hinv, const int* sched, int n, int d, int F, int T, int K, int splits,
+                                float* P2, KStatus st, int num_sms, cudaStream_t s);
 
 // self-test of the bounded waits -------------------------------------------------
 cudaError_t launch_wait_selftest(KStatus st, cudaStream_t s);

@@ -22,6 +22,8 @@ struct moe_ctx {
     int force_path = 0;
     int gemm_pair = 0;          // 0 auto, 1 single CTA, 2 CTA pairs
     int host_out = 1;           // moe_forward_host: 1 = kernels write y into pinned host memory directly
+    int fp8_widen = 0;          // moe_forward_fp8: 0 = e4m3 MMA on split token rows, 1 = weights widened to bf16
+    int decode_fused = 0;       // bf16 weight streaming: 1 = the one-kernel path (decode_fused.cu), 0 = five kernels
     int device = 0;
     int num_sms = 148;
     int* status_host = nullptr;   // host-mapped
@@ -37,6 +39,7 @@ struct moe_ctx {
     int32_t* inv = nullptr;
     int* sched = nullptr;
     int* xchg = nullptr;        // grid-barrier words and block counts of the fused routing kernel
+    int* fbar = nullptr;        // grid-barrier words of the one-kernel decode path
     int* ccnt = nullptr;        // [T][d/128] arrival counters of the combine fused into the W2 epilogue
     float* rstd = nullptr;      // [T] 1/rms of each row (residual blocks: RMSNorm before routing)
     void* Xp = nullptr;
@@ -53,12 +56,16 @@ struct moe_ctx {
     float* Pa = nullptr;        // decode partial sums [S][R][F] (W1 rows), [S][R][F] (W3 rows)
     float* Pb = nullptr;
     float* P2 = nullptr;        // decode partial sums [S][R][d] (W2 rows)
+    uint8_t* Xq = nullptr;      // e4m3 MMA path: hi/lo e4m3 token rows [2R][d] and SwiGLU rows [2R][F],
+    uint8_t* Hq = nullptr;      //   with 1/scale per row
+    float* xinv = nullptr;
+    float* hinv = nullptr;
     CUtensorMap map_Xp, map_H, map_Xp32, map_H32;
     bool maps_ok = false;
     // per-stage CUDA-event timing (MOE_OPT_STAGE_TIMING)
     bool stage_timing = false;
     std::vector<cudaEvent_t> ev_free;
-    std::vector<std::array<cudaEvent_t, 5>> ev_calls;
+    std::vector<std::array<cudaEvent_t, 6>> ev_calls;
 };
 
 namespace {
@@ -67,7 +74,8 @@ size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, rstd, Xp, H, Ys, xbuf, xbuf2, ybuf, Pa, Pb, P2, total;
+    size_t topk_idx, topk_w, perm, inv, sched, xchg, fbar, ccnt, rstd, Xp, H, Ys, xbuf, xbuf2, ybuf, Pa, Pb, P2, Xq,
+        Hq, xinv, hinv, total;
 };
 
 Layout layout_for(const moe_ctx* c, int T, int Tdec) {
@@ -83,6 +91,7 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.inv = take(R * 4);
     L.sched = take(static_cast<size_t>(sched_ints(c->n)) * 4);
     L.xchg = take(static_cast<size_t>(fused_route_xchg_ints()) * 4);
+    L.fbar = take(static_cast<size_t>(fused_decode_bar_ints()) * 4);
     L.ccnt = take(Tn * static_cast<size_t>((c->d + 127) / 128) * 4);
     L.rstd = take(Tn * 4);
     L.Xp = take(R * c->d * es);
@@ -95,6 +104,10 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.Pa = take(kDecodeMaxSplits * Rd * c->F * 4);
     L.Pb = take(kDecodeMaxSplits * Rd * c->F * 4);
     L.P2 = take(kDecodeMaxSplits * Rd * c->d * 4);
+    L.Xq = take(c->dtype == MOE_BF16 ? 2 * Rd * c->d : 0);
+    L.Hq = take(c->dtype == MOE_BF16 ? 2 * Rd * c->F : 0);
+    L.xinv = take(Rd * 4);
+    L.hinv = take(kDecodeMaxSplits * Rd * 4);
     L.total = off;
     return L;
 }
@@ -152,6 +165,7 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->inv = reinterpret_cast<int32_t*>(b + L.inv);
     c->sched = reinterpret_cast<int*>(b + L.sched);
     c->xchg = reinterpret_cast<int*>(b + L.xchg);
+    c->fbar = reinterpret_cast<int*>(b + L.fbar);
     c->ccnt = reinterpret_cast<int*>(b + L.ccnt);
     c->rstd = reinterpret_cast<float*>(b + L.rstd);
     c->Xp = b + L.Xp;
@@ -163,6 +177,10 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->Pa = reinterpret_cast<float*>(b + L.Pa);
     c->Pb = reinterpret_cast<float*>(b + L.Pb);
     c->P2 = reinterpret_cast<float*>(b + L.P2);
+    c->Xq = reinterpret_cast<uint8_t*>(b + L.Xq);
+    c->Hq = reinterpret_cast<uint8_t*>(b + L.Hq);
+    c->xinv = reinterpret_cast<float*>(b + L.xinv);
+    c->hinv = reinterpret_cast<float*>(b + L.hinv);
     c->cap_T = T;
     c->cap_dec = Tdec;
     if (cudaMemsetAsync(c->xchg, 0, L.rstd - L.xchg, s) != cudaSuccess) return MOE_ERR_CUDA;   // every counter region
@@ -223,24 +241,25 @@ bool use_decode(const moe_ctx* c, int T) {
 bool use_pair13(const moe_ctx* c) { return c->gemm_pair == 2 && pair_gemm_available(c->num_sms); }
 bool use_pair2(const moe_ctx* c) { return c->gemm_pair != 1 && pair_gemm_available(c->num_sms); }
 
-// Stages of one forward call, in launch order.
-constexpr int kStages = 4;
-const char* const kStageNames[kStages] = {"route", "expert_w1w3_swiglu", "expert_w2_gate", "combine"};
+// Stages of one forward call, in launch order.  The five-kernel and grouped
+// paths run stages 0-3; the one-kernel decode path runs stage 4 alone.
+constexpr int kStages = 5;
+const char* const kStageNames[kStages] = {"route", "expert_w1w3_swiglu", "expert_w2_gate", "combine",
+                                          "decode_fused"};
 
-// Stage boundaries of the current call: an NVTX range per stage on the host
-// thread that launches it (named as the stages of moe_stage_times, nested in
-// one range for the call), and CUDA events on the call's stream when stage
-// timing is on.
+// Stage boundaries of the current call: an NVTX range for the call and, inside
+// it, one per stage that runs, on the host thread that launches them; CUDA
+// events on the call's stream when stage timing is on (stages that do not run
+// get zero-length intervals).
 struct StageMarks {
     moe_ctx* c = nullptr;
     cudaStream_t s = nullptr;
-    std::array<cudaEvent_t, 5> ev{};
+    std::array<cudaEvent_t, kStages + 1> ev{};
     bool on = false;
-    int nvtx_depth = 0;
+    int next = 0;             // events ev[0 .. next) recorded
+    bool range_open = false;
     StageMarks(moe_ctx* ctx, cudaStream_t st, const char* call = "moe_forward") : c(ctx), s(st) {
         nvtxRangePushA(call);
-        nvtxRangePushA(kStageNames[0]);
-        nvtx_depth = 2;
         if (!c->stage_timing) return;
         for (int i = 0; i <= kStages; ++i) {
             if (!c->ev_free.empty()) {
@@ -253,26 +272,30 @@ struct StageMarks {
         }
         on = true;
         cudaEventRecord(ev[0], s);
+        next = 1;
     }
-    void mark(int stage) {
-        if (nvtx_depth == 2) {
-            nvtxRangePop();
-            if (stage + 1 < kStages) {
-                nvtxRangePushA(kStageNames[stage + 1]);
-            } else {
-                nvtx_depth = 1;
-            }
-        }
-        if (on) cudaEventRecord(ev[stage + 1], s);
+    // The launches from here on belong to stage i.
+    void begin(int i) {
+        if (range_open) nvtxRangePop();
+        nvtxRangePushA(kStageNames[i]);
+        range_open = true;
+        if (on)
+            while (next <= i) cudaEventRecord(ev[next++], s);
     }
     void finish() {
+        if (range_open) {
+            nvtxRangePop();
+            range_open = false;
+        }
         if (on) {
+            while (next <= kStages) cudaEventRecord(ev[next++], s);
             c->ev_calls.push_back(ev);
             on = false;
         }
     }
     ~StageMarks() {
-        while (nvtx_depth-- > 0) nvtxRangePop();
+        if (range_open) nvtxRangePop();
+        nvtxRangePop();
         if (on)
             for (int i = 0; i <= kStages; ++i) c->ev_free.push_back(ev[i]);
     }
@@ -289,6 +312,54 @@ int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s,
     return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+// The one-kernel decode path (decode_fused.cu): everything of the layer in one
+// cooperative launch.  Returns MOE_ERR_UNSUPPORTED (nothing launched) when the
+// device cannot hold the grid, so that the caller can run the five kernels.
+int run_decode_fused(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2,
+                     void* y, int T, cudaStream_t s, float norm_eps, const void* resid, StageMarks& marks) {
+    CUtensorMap mW1, mW3, mW2;
+    const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
+    if (!encode_map_bf16_2d(&mW1, W1, nF, c->d, 128) || !encode_map_bf16_2d(&mW3, W3, nF, c->d, 128) ||
+        !encode_map_bf16_2d(&mW2, W2, nd, c->F, 128))
+        return MOE_ERR_CUDA;
+    FusedDecodeInput in{};
+    in.x = static_cast<const __nv_bfloat16*>(x);
+    in.Wg = Wg;
+    in.bias = c->bias;
+    in.resid = static_cast<const __nv_bfloat16*>(resid);
+    in.y = static_cast<__nv_bfloat16*>(y);
+    in.T = T;
+    in.d = c->d;
+    in.F = c->F;
+    in.n = c->n;
+    in.K = c->k;
+    in.norm_eps = norm_eps;
+    in.topk_idx = c->topk_idx;
+    in.topk_w = c->topk_w;
+    in.rstd = norm_eps >= 0.0f ? c->rstd : nullptr;
+    in.sched = c->sched;
+    in.perm = c->perm;
+    in.inv = c->inv;
+    in.Xp = static_cast<__nv_bfloat16*>(c->Xp);
+    in.H = static_cast<__nv_bfloat16*>(c->H);
+    in.Pa = c->Pa;
+    in.Pb = c->Pb;
+    in.P2 = c->P2;
+    in.bar = c->fbar;
+    in.st = kstatus(c);
+    cudaError_t e = prepare_decode_fused(in, c->num_sms);
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        return MOE_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.begin(kStages - 1);
+    e = launch_decode_fused(mW1, mW3, mW2, c->map_Xp32, c->map_H32, in, c->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    marks.finish();
+    return MOE_OK;
+}
+
 // y = MoE(x); with norm_eps >= 0 and resid: y = resid + MoE(RMSNorm(x)) (the
 // residual block of a stack, x == resid == y allowed).
 int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
@@ -296,17 +367,22 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
     const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
     const int R = c->k * T;
     StageMarks marks(c, s);
+    if (et == ElemType::BF16 && use_decode(c, T) && c->decode_fused &&
+        fused_decode_supported(T, c->d, c->F, c->n, c->k, c->num_sms)) {
+        const int rc = run_decode_fused(c, x, Wg, W1, W3, W2, y, T, s, norm_eps, resid, marks);
+        if (rc != MOE_ERR_UNSUPPORTED) return rc;
+    }
+    marks.begin(0);
     int rc = run_route(c, x, Wg, T, s, nullptr, true, norm_eps);
     if (rc != MOE_OK) return rc;
-    marks.mark(0);
     cudaError_t e = cudaSuccess;
     if (et == ElemType::F32) {
+        marks.begin(1);
         e = launch_simt_gemm13(et, c->Xp, W1, W3, c->H, c->sched, c->n, c->d, c->F, R, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(1);
+        marks.begin(2);
         e = launch_simt_gemm2(et, c->H, W2, c->Ys, c->sched, c->perm, c->topk_w, c->n, c->d, c->F, R, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(2);
     } else if (use_decode(c, T)) {
         CUtensorMap mW1, mW3, mW2;
         const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
@@ -317,18 +393,18 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         const int touched = c->n < R ? c->n : R;
         const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 64, c->num_sms);
         const int s1 = decode_pick_splits(touched * (c->d / 128), c->F / 64, c->num_sms);
+        marks.begin(1);
         e = launch_decode_w13(mW1, mW3, c->map_Xp32, c->sched, c->n, c->d, c->F, T, c->k, s0, c->Pa, c->Pb, st,
                               c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
         e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(1);
+        marks.begin(2);
         e = launch_decode_w2(mW2, c->map_H32, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(2);
+        marks.begin(3);
         e = launch_decode_combine(et, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, resid, y, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(3);
         marks.finish();
         return MOE_OK;
     } else {
@@ -343,6 +419,7 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         CUtensorMap mW1h, mW3h;
         if (pair13 && (!encode_map_bf16_2d(&mW1h, W1, nF, c->d, 64) || !encode_map_bf16_2d(&mW3h, W3, nF, c->d, 64)))
             return MOE_ERR_CUDA;
+        marks.begin(1);
         if (pair13)
             e = launch_pair_gemm13(c->map_Xp, mW1, mW3, mW1h, mW3h, c->sched, c->n, c->d, c->F, R,
                                    static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
@@ -350,7 +427,6 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
             e = launch_tc_gemm13(c->map_Xp, mW1, mW3, c->sched, c->n, c->d, c->F, R,
                                  static_cast<__nv_bfloat16*>(c->H), st, c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(1);
         CombineArgs comb{};
         comb.cnt = c->ccnt;
         comb.y = static_cast<__nv_bfloat16*>(y);
@@ -358,6 +434,7 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         comb.K = c->k;
         comb.nblk = c->d / 128;
         comb.d = c->d;
+        marks.begin(2);
         if (pair2)
             e = launch_pair_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, comb, st,
                                   c->num_sms, s);
@@ -365,51 +442,74 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
             e = launch_tc_gemm2(c->map_H, mW2, c->sched, c->n, c->d, c->F, R, c->Ys, c->perm, c->topk_w, comb, st,
                                 c->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
-        marks.mark(2);
-        marks.mark(3);   // the combine ran inside the W2 epilogue
+        marks.begin(3);   // the combine ran inside the W2 epilogue
         marks.finish();
         return MOE_OK;
     }
+    marks.begin(3);
     e = launch_combine(et, c->Ys, T, c->k, c->d, resid, y, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(3);
     marks.finish();
     return MOE_OK;
 }
 
 // y = MoE(x) for T <= kDecodeMaxT tokens with e4m3 expert weights and fp32
-// row scales: the weight-streaming path with the fp8 GEMM kernels, same split
-// choice, SwiGLU and combine kernels as the bf16 one.
+// row scales: the weight-streaming path, same split choice and combine kernel
+// as the bf16 one.  By default the weights meet the tokens in the e4m3 MMA
+// (token rows split into hi/lo e4m3 rows, decode_fp8_mma.cu); with
+// MOE_OPT_FP8_WIDEN the weights are widened to bf16 on chip (decode_fp8.cu).
 int run_forward_fp8(moe_ctx* c, const void* x, const float* Wg, const uint8_t* W1q, const float* W1s,
                     const uint8_t* W3q, const float* W3s, const uint8_t* W2q, const float* W2s, void* y, int T,
                     cudaStream_t s) {
     const int R = c->k * T;
     StageMarks marks(c, s, "moe_forward_fp8");
+    marks.begin(0);
     int rc = run_route(c, x, Wg, T, s, nullptr, true);
     if (rc != MOE_OK) return rc;
-    marks.mark(0);
     CUtensorMap mW1, mW3, mW2;
     const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
-    if (!encode_map_u8_sw64(&mW1, W1q, nF, c->d) || !encode_map_u8_sw64(&mW3, W3q, nF, c->d) ||
-        !encode_map_u8_sw64(&mW2, W2q, nd, c->F))
-        return MOE_ERR_CUDA;
     const KStatus st = kstatus(c);
     const int touched = c->n < R ? c->n : R;
-    const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 64, c->num_sms);
-    const int s1 = decode_pick_splits(touched * (c->d / 128), c->F / 64, c->num_sms);
-    cudaError_t e = launch_decode_fp8_w13(mW1, mW3, c->map_Xp32, W1s, W3s, c->sched, c->n, c->d, c->F, T, c->k, s0,
-                                          c->Pa, c->Pb, st, c->num_sms, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(1);
-    e = launch_decode_fp8_w2(mW2, c->map_H32, W2s, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms,
-                             s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(2);
+    cudaError_t e = cudaSuccess;
+    int s1 = 1;
+    if (!c->fp8_widen) {
+        CUtensorMap mXq, mHq;
+        if (!encode_map_u8_sw128(&mW1, W1q, nF, c->d, 128) || !encode_map_u8_sw128(&mW3, W3q, nF, c->d, 128) ||
+            !encode_map_u8_sw128(&mW2, W2q, nd, c->F, 128) ||
+            !encode_map_u8_sw128(&mXq, c->Xq, 2ull * R, c->d, 64) || !encode_map_u8_sw128(&mHq, c->Hq, 2ull * R, c->F, 64))
+            return MOE_ERR_CUDA;
+        const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 128, c->num_sms);
+        s1 = decode_pick_splits(touched * (c->d / 128), c->F / 128, c->num_sms);
+        marks.begin(1);
+        e = launch_split_rows_e4m3(static_cast<const __nv_bfloat16*>(c->Xp), R, c->d, c->Xq, c->xinv, s);
+        if (e == cudaSuccess)
+            e = launch_decode_f8_w13(mW1, mW3, mXq, W1s, W3s, c->xinv, c->sched, c->n, c->d, c->F, T, c->k, s0, c->Pa,
+                                     c->Pb, st, c->num_sms, s);
+        if (e == cudaSuccess) e = launch_decode_swiglu_split(c->Pa, c->Pb, s0, R, c->F, s1, c->Hq, c->hinv, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.begin(2);
+        e = launch_decode_f8_w2(mW2, mHq, W2s, c->hinv, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st,
+                                c->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    } else {
+        if (!encode_map_u8_sw64(&mW1, W1q, nF, c->d) || !encode_map_u8_sw64(&mW3, W3q, nF, c->d) ||
+            !encode_map_u8_sw64(&mW2, W2q, nd, c->F))
+            return MOE_ERR_CUDA;
+        const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 64, c->num_sms);
+        s1 = decode_pick_splits(touched * (c->d / 128), c->F / 64, c->num_sms);
+        marks.begin(1);
+        e = launch_decode_fp8_w13(mW1, mW3, c->map_Xp32, W1s, W3s, c->sched, c->n, c->d, c->F, T, c->k, s0, c->Pa,
+                                  c->Pb, st, c->num_sms, s);
+        if (e == cudaSuccess) e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        marks.begin(2);
+        e = launch_decode_fp8_w2(mW2, c->map_H32, W2s, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st,
+                                 c->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    marks.begin(3);
     e = launch_decode_combine(ElemType::BF16, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, nullptr, y, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    marks.mark(3);
     marks.finish();
     return MOE_OK;
 }
@@ -496,6 +596,14 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
         case MOE_OPT_STAGE_TIMING:
             if (value < 0 || value > 1) return MOE_ERR_INVALID;
             c->stage_timing = value != 0;
+            return MOE_OK;
+        case MOE_OPT_FP8_WIDEN:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID;
+            c->fp8_widen = static_cast<int>(value);
+            return MOE_OK;
+        case MOE_OPT_DECODE_FUSED:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID;
+            c->decode_fused = static_cast<int>(value);
             return MOE_OK;
         default:
             return MOE_ERR_INVALID;

@@ -57,14 +57,6 @@ constexpr int FR_WARPS = 16;
 constexpr int FR_DS_LARGE = 4;              // warps that split one row (batches of many tokens)
 constexpr int FR_ROUND = FR_THREADS;        // assignments placed per round in phase 2
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 }  // namespace
 
 struct FusedRouteArgs {
@@ -87,105 +79,6 @@ struct FusedRouteArgs {
     float* rstd;            // NORM: [T] 1 / rms of each row, for the gather
     KStatus st;
 };
-
-// x * s rounded to the element type (bf16: round to nearest even; fp32: as is).
-template <typename TX>
-__device__ __forceinline__ float scale_round(float x, float s) {
-    if constexpr (sizeof(TX) == 2) return __bfloat162float(__float2bfloat16_rn(x * s));
-    return x * s;
-}
-
-// Sum over the 32 lanes of V values per lane (V a power of two).  Each step
-// trades half of the values with the partner lane and adds, halving the count,
-// until one value per lane is left; remaining steps are plain butterflies.
-// Afterwards lane l holds the full sums of value indices fr_index(l, i),
-// i < max(V/32, 1).
-template <int V>
-__device__ __forceinline__ void lane_transpose_sum(float (&v)[V], int lane) {
-    int cur = V;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        if (cur > 1) {
-            const int half = cur >> 1;
-            const bool up = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < V / 2; ++i) {
-                if (i < half) {
-                    const float send = up ? v[i] : v[half + i];
-                    const float keep = up ? v[half + i] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            }
-            cur = half;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-        }
-    }
-}
-// 4 consecutive elements of a row as loaded (bf16: 8 bytes, fp32: 16 bytes),
-// so that the next segment's loads can be in flight while one is computed.
-template <typename TX>
-struct Raw4;
-template <>
-struct Raw4<__nv_bfloat16> {
-    uint2 v;
-};
-template <>
-struct Raw4<float> {
-    float4 v;
-};
-template <typename TX>
-__device__ __forceinline__ void load_raw4(const TX* row, int j0, bool ok, Raw4<TX>& r) {
-    if constexpr (sizeof(TX) == 2) {
-        r.v = ok ? __ldg(reinterpret_cast<const uint2*>(row + j0)) : make_uint2(0u, 0u);
-    } else {
-        r.v = ok ? __ldg(reinterpret_cast<const float4*>(row + j0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-}
-template <typename TX>
-__device__ __forceinline__ void unpack_raw4(const Raw4<TX>& r, float* v) {
-    if constexpr (sizeof(TX) == 2) {
-        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&r.v.x);
-        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&r.v.y);
-        v[0] = __low2float(lo);
-        v[1] = __high2float(lo);
-        v[2] = __low2float(hi);
-        v[3] = __high2float(hi);
-    } else {
-        v[0] = r.v.x; v[1] = r.v.y; v[2] = r.v.z; v[3] = r.v.w;
-    }
-}
-
-// 16 bytes of a row (8 bf16 or 4 fp32), each element times s, rounded back.
-template <typename TX>
-__device__ __forceinline__ uint4 scale_row_vec(uint4 v, float s) {
-    if constexpr (sizeof(TX) == 2) {
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-            const __nv_bfloat162 o = __floats2bfloat162_rn(__low2float(b) * s, __high2float(b) * s);
-            w[i] = *reinterpret_cast<const uint32_t*>(&o);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-        return make_uint4(__float_as_uint(__uint_as_float(v.x) * s), __float_as_uint(__uint_as_float(v.y) * s),
-                          __float_as_uint(__uint_as_float(v.z) * s), __float_as_uint(__uint_as_float(v.w) * s));
-    }
-}
-
-template <int V>
-__device__ __forceinline__ int fr_index(int lane, int i) {
-    int idx = i, cur = V;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        if (cur > 1) {
-            cur >>= 1;
-            if (lane & o) idx += cur;
-        }
-    }
-    return idx;
-}
 
 // SMALL (one token per block, small batches): all 16 warps split the row and
 // W_g is read from L2 instead of being staged in shared memory first, which

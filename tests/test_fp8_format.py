@@ -108,3 +108,39 @@ def test_widening_recipe_against_the_format():
     assert np.array_equal(v_hi, oracle.decode_e4m3(b1.astype(np.uint8)))
     # the sign of zero survives too
     assert np.array_equal(np.signbit(v_lo), np.signbit(oracle.decode_e4m3(b0.astype(np.uint8))))
+
+
+def split_recipe(v: np.ndarray):
+    """The e4m3-MMA kernels' token split, restated on the host: for a row v (bf16
+    values), s = 2^k with max|v| * s in (224, 448]; hi = e4m3(s v), lo = e4m3(s v - hi),
+    e4m3 rounding to nearest even (torch's conversion).  Returns (s, hi, lo) as
+    exact fp64 values (the byte values through the oracle's decoding)."""
+    mx = float(np.max(np.abs(v)))
+    m, e = np.frexp(448.0 / mx)                 # 448/mx = m 2^e, 0.5 <= m < 1
+    s = 2.0 ** (e - 1)                          # the largest power of two <= 448/mx
+    sv = torch.from_numpy((v * s).astype(np.float32))
+    hi_b = sv.to(torch.float8_e4m3fn)
+    hi = hi_b.float()
+    lo_b = (sv - hi).to(torch.float8_e4m3fn)
+    dec = lambda b: oracle.decode_e4m3(b.view(torch.uint8).numpy())
+    return s, dec(hi_b), dec(lo_b)
+
+
+def test_token_split_recipe_is_exact_above_a_quarter():
+    """Every bf16 value is hi + lo of two e4m3 values after the row's power-of-two
+    scale, exactly when |s v| >= 1/4, and within 2^-10 (half of e4m3's smallest
+    step) below; the scale puts the row's largest magnitude in (224, 448]."""
+    # every finite bf16 bit pattern of magnitude in [2^-30, 448), as rows under
+    # several row maxima
+    bits = np.arange(0, 1 << 16, dtype=np.uint32)
+    v = (bits << 16).view(np.float32).astype(np.float64)
+    v = v[np.isfinite(v) & (np.abs(v) < 448.0) & ((np.abs(v) >= 2.0 ** -30) | (v == 0.0))]
+    for row_max in (1.0, 3.75, 4.5, 100.0, 447.0):
+        row = np.concatenate([v[np.abs(v) <= row_max], [row_max]])
+        s, hi, lo = split_recipe(row)
+        assert 224.0 < np.max(np.abs(row)) * s <= 448.0
+        sv = row * s
+        err = np.abs(hi + lo - sv)
+        big = np.abs(sv) >= 0.25
+        assert np.all(err[big] == 0.0)
+        assert np.all(err[~big] <= 2.0 ** -10)

@@ -1,9 +1,14 @@
-"""moe_forward_fp8 (e4m3 expert weights, fp32 row scales) on the GPU.
+"""moe_forward_fp8 (e4m3 expert weights, fp32 row scales) on the GPU, both kernels.
 
-With power-of-two scales the dequantised weights s * q are exact in bf16, and
-the fp8 kernels must then reproduce, bit for bit, the bf16 weight-streaming
-path run on those weights; both are checked against the fp64 oracle on the
-oracle's own dequantisation of the bytes."""
+* Default (MOE_OPT_FP8_WIDEN = 0): the weight bytes go straight into the e4m3
+  tensor-core MMA against token rows split into hi/lo e4m3 rows.  Checked
+  against the fp64 oracle on the oracle's own dequantisation of the bytes, and
+  against the bf16 path on the dequantised weights, both within the bf16 bound.
+* Widening (MOE_OPT_FP8_WIDEN = 1): with power-of-two scales the dequantised
+  weights s * q are exact in bf16, and the kernels must reproduce, bit for bit,
+  the bf16 weight-streaming path run on those weights; also checked against the
+  oracle.
+"""
 import numpy as np
 import pytest
 import torch
@@ -45,9 +50,10 @@ def oracle_y(x, Wg, bias, q, s, K, toks, gpu_idx):
     return oracle.moe_tokens(xo, *W, idx_u, gate_u, toks), logits, idx, gate
 
 
-def run_both(w, layer, q, s):
+def run_both(w, layer, q, s, widen=1):
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=layer["bias"])
     m.set_option(_lib.MOE_OPT_FORCE_PATH, 2)
+    m.set_option(_lib.MOE_OPT_FP8_WIDEN, widen)
     r = m.route(layer["x"], layer["Wg"])
     y8 = m.forward_fp8(layer["x"], layer["Wg"], q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     deq = {n: inputs.dequantize_e4m3_rows(q[n], s[n]) for n in NAMES}
@@ -73,36 +79,57 @@ FP8_CASES = [
 
 
 @pytest.mark.parametrize("T,d,F,n,K", FP8_CASES)
-def test_fp8_equals_bf16_on_dequantised_weights(T, d, F, n, K):
+def test_fp8_widened_equals_bf16_on_dequantised_weights(T, d, F, n, K):
     w = inputs.Workload("fp8", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=300 + T + d)
     layer = inputs.make_layer(w, "cuda")
     q, s = quantize_layer(layer)
-    m, y8, y16, gidx, gw = run_both(w, layer, q, s)
+    m, y8, y16, gidx, gw = run_both(w, layer, q, s, widen=1)
     assert torch.equal(y8, y16)
     y_ref, logits, idx, gate = oracle_y(layer["x"], layer["Wg"], layer["bias"], q, s, K, np.arange(T), gidx)
     check_route(gidx, gw, logits, idx, gate, K)
     assert_close(y_to_numpy(y8), y_ref, "bf16")
 
 
-def test_fp8_all_tokens_to_one_expert_pair_and_deterministic():
-    # 200 tokens on experts (5, 2): N = 224 token columns per item; W1 and W3 run as separate items
+@pytest.mark.parametrize("T,d,F,n,K", FP8_CASES)
+def test_fp8_mma_matches_oracle_and_bf16_path(T, d, F, n, K):
+    w = inputs.Workload("fp8", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=300 + T + d)
+    layer = inputs.make_layer(w, "cuda")
+    q, s = quantize_layer(layer)
+    m, y8, y16, gidx, gw = run_both(w, layer, q, s, widen=0)
+    y_ref, logits, idx, gate = oracle_y(layer["x"], layer["Wg"], layer["bias"], q, s, K, np.arange(T), gidx)
+    check_route(gidx, gw, logits, idx, gate, K)
+    err, bound = assert_close(y_to_numpy(y8), y_ref, "bf16")
+    assert_close(y_to_numpy(y8), y_to_numpy(y16), "bf16")
+    print(f"fp8 e4m3 MMA T={T} d={d} F={F} n={n} K={K}: max err {err:.3e} (bound {bound:.3e})")
+
+
+@pytest.mark.parametrize("widen", [0, 1])
+def test_fp8_all_tokens_to_one_expert_pair_and_deterministic(widen):
+    # 200 tokens on experts (5, 2): 224 token columns per item (448 hi/lo columns,
+    # two MMAs per K step, for the e4m3 MMA); W1 and W3 run as separate items
     w = inputs.Workload("fp8_skew", T=200, d=256, d_ff=384, bias=(0, 0, 50, 0, 0, 100, 0, 0), seed=8)
     layer = inputs.make_layer(w, "cuda")
     q, s = quantize_layer(layer)
-    m, y8, y16, gidx, _ = run_both(w, layer, q, s)
+    m, y8, y16, gidx, gw = run_both(w, layer, q, s, widen=widen)
     assert np.all(gidx == [5, 2])
-    assert torch.equal(y8, y16)
+    if widen:
+        assert torch.equal(y8, y16)
+    else:
+        y_ref, *_ = oracle_y(layer["x"], layer["Wg"], layer["bias"], q, s, w.k, np.arange(w.T), gidx)
+        assert_close(y_to_numpy(y8), y_ref, "bf16")
     y8b = m.forward_fp8(layer["x"], layer["Wg"], q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     assert torch.equal(y8, y8b)
 
 
-def test_fp8_scales_not_powers_of_two():
+@pytest.mark.parametrize("widen", [0, 1])
+def test_fp8_scales_not_powers_of_two(widen):
     # s * 0.75: the row scale multiplies the fp32 accumulator (one rounding), so
     # only the tolerance against the oracle holds, not bitwise equality
     w = inputs.Workload("fp8_s", T=48, d=512, d_ff=384, seed=44)
     layer = inputs.make_layer(w, "cuda")
     q, s = quantize_layer(layer, scale_factor=0.75)
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=layer["bias"])
+    m.set_option(_lib.MOE_OPT_FP8_WIDEN, widen)
     r = m.route(layer["x"], layer["Wg"])
     y8 = m.forward_fp8(layer["x"], layer["Wg"], q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     torch.cuda.synchronize()
@@ -112,12 +139,14 @@ def test_fp8_scales_not_powers_of_two():
     assert_close(y_to_numpy(y8), y_ref, "bf16")
 
 
-def test_fp8_batches_above_256_run_in_chunks():
+@pytest.mark.parametrize("widen", [0, 1])
+def test_fp8_batches_above_256_run_in_chunks(widen):
     # 600 tokens = chunks of 256, 256, 88; each chunk equals a separate call
     w = inputs.Workload("fp8_chunks", T=600, d=256, d_ff=256, seed=12)
     layer = inputs.make_layer(w, "cuda")
     q, s = quantize_layer(layer)
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=layer["bias"])
+    m.set_option(_lib.MOE_OPT_FP8_WIDEN, widen)
     args = (layer["Wg"], q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     y = m.forward_fp8(layer["x"], *args)
     parts = [m.forward_fp8(layer["x"][a:b].contiguous(), *args) for a, b in ((0, 256), (256, 512), (512, 600))]
@@ -184,21 +213,25 @@ def mixtral_fp8():
 
 @pytest.mark.parametrize("T", [1, 8, 32, 128, 256])
 def test_mixtral_decode_fp8(mixtral_fp8, T):
-    """Mixtral shape, every token: bitwise equal to the bf16 weight-streaming path
-    on the dequantised weights, and within the bf16 bound of the oracle run on
-    its own decoding of the e4m3 bytes."""
+    """Mixtral shape, every token, both kernels against the oracle run on its own
+    decoding of the e4m3 bytes; the widening kernel bitwise equal to the bf16
+    weight-streaming path on the dequantised weights, the e4m3 MMA within the
+    bf16 bound of it."""
     w, q, s, host = mixtral_fp8
     x = inputs.make_x(w, "cuda", seed=None if T == 32 else 60 + T, T=T)
     Wg, b = inputs.make_router(w, "cuda")
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=b)
     m.set_option(_lib.MOE_OPT_FORCE_PATH, 2)
     r = m.route(x, Wg)
-    y8 = m.forward_fp8(x, Wg, q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
+    ys = {}
+    for widen in (0, 1):
+        m.set_option(_lib.MOE_OPT_FP8_WIDEN, widen)
+        ys[widen] = m.forward_fp8(x, Wg, q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     deq = {n: inputs.dequantize_e4m3_rows(q[n], s[n]) for n in NAMES}
     y16 = m.forward(x, Wg, deq["W1"], deq["W3"], deq["W2"])
     torch.cuda.synchronize()
     assert m.status() == 0
-    assert torch.equal(y8, y16)
+    assert torch.equal(ys[1], y16)
     del deq
     gidx, gw = r["topk_idx"].cpu().numpy(), r["topk_w"].cpu().numpy()
     xo, Wgo, bo = inputs.to_oracle(x), inputs.to_oracle(Wg), inputs.to_oracle(b)
@@ -207,6 +240,9 @@ def test_mixtral_decode_fp8(mixtral_fp8, T):
     near = check_route(gidx, gw, logits, idx, gate, w.k)
     idx_u, gate_u, _ = reference_selection(dict(logits=logits, idx=idx, gate=gate), gidx, w.k)
     y_ref = oracle.moe_tokens(xo, *host, idx_u, gate_u, np.arange(T))
-    err, bound = assert_close(y_to_numpy(y8), y_ref, "bf16")
-    print(f"fp8 decode T={T}: max err {err:.3e} (bound {bound:.3e}), near ties {near}")
+    for widen in (0, 1):
+        err, bound = assert_close(y_to_numpy(ys[widen]), y_ref, "bf16")
+        print(f"fp8 decode T={T} {'widened' if widen else 'e4m3 MMA'}: max err {err:.3e} (bound {bound:.3e}), "
+              f"near ties {near}")
+    assert_close(y_to_numpy(ys[0]), y_to_numpy(y16), "bf16")
     m.close()
