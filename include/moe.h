@@ -35,8 +35,8 @@
  *    never used as an address) are recorded in a sticky status word that
  *    moe_status() reads without synchronising.
  *  - Each forward call is one NVTX range on the calling host thread ("moe_forward"
- *    or "moe_forward_fp8") holding one nested range per stage it runs, named
- *    as the stages of moe_stage_times; a profiler that records NVTX shows them.
+ *    or "moe_forward_fp8") holding one nested range per stage, named as the
+ *    stages of moe_stage_times; a profiler that records NVTX shows them.
  *  - A context must not be used from two host threads at once; calls on
  *    different streams with the same context share its workspace and must be
  *    ordered by the caller.
@@ -81,13 +81,9 @@ typedef enum {
     MOE_OPT_HOST_OUTPUT = 6,   /* moe_forward_host: 1 = when y_host is pinned, the layer's last kernel writes y
                                   into it directly over the bus (default; measured 0.19 ms faster per call at
                                   T=4096), 0 = always copy y back on the stream */
-    MOE_OPT_FP8_WIDEN = 7,     /* moe_forward_fp8: 0 = e4m3 weights into the 8-bit MMA against split token rows
+    MOE_OPT_FP8_WIDEN = 7      /* moe_forward_fp8: 0 = e4m3 weights into the 8-bit MMA against split token rows
                                   (default), 1 = weights widened to bf16 on chip (bitwise equal to the bf16
                                   path on the dequantised weights; slower) */
-    MOE_OPT_DECODE_FUSED = 8   /* bf16 weight-streaming path: 0 = the routing, W1/W3, SwiGLU, W2 and combine
-                                  kernels (default), 1 = the whole layer in one cooperative kernel when
-                                  T <= the number of SMs, T*k <= 512 and the device holds one CTA per SM
-                                  (same result bit for bit; measured slower, see moe_forward) */
 } moe_option_t;
 
 /*
@@ -153,11 +149,7 @@ int moe_router_logits(moe_ctx* ctx, const void* x, const float* W_g, int T, floa
  * adds each token's k expert rows in slot order (replacing index_add_,
  * aiqianji 3.1.2) with no atomics, so results are bitwise reproducible.
  * bf16: fp32 accumulation, the SwiGLU product rounded once to bf16, y rounded
- * once.  Small T (<= MOE_OPT_DECODE_MAX_T) uses weight-streaming kernels;
- * with MOE_OPT_DECODE_FUSED the whole layer runs instead as one cooperative
- * kernel with one CTA per SM, which gives the same result bit for bit (but
- * measured slower: its SwiGLU and combine steps run on one CTA per SM and
- * wait on more L2 round trips than the separate kernels' full grids).
+ * once.  Small T (<= MOE_OPT_DECODE_MAX_T) uses weight-streaming kernels.
  * x and y must not overlap.  T == 0 is a no-op.
  */
 int moe_forward(moe_ctx* ctx, const void* x, const float* W_g, const void* W1, const void* W3,
@@ -268,9 +260,8 @@ int moe_selftest_wait_timeout(moe_ctx* ctx, long long wait_limit_us, moe_stream_
  * call of each stage into ms[0..max_stages) (stage names: moe_stage_name) and
  * the number of calls into *calls, then forgets the recorded calls.  Returns
  * the number of stages (>= 0) or a negative moe_status_t.  Stages: "route",
- * "expert_w1w3_swiglu", "expert_w2_gate", "combine" (the grouped and the
- * five-kernel decode paths) and "decode_fused" (the one-kernel decode path);
- * a stage a call does not run counts zero for that call.
+ * "expert_w1w3_swiglu" (with the decode path's SwiGLU kernel), "expert_w2_gate"
+ * and "combine" (zero-length on the grouped path, whose W2 epilogue combines).
  */
 int moe_stage_times(moe_ctx* ctx, float* ms, int max_stages, int* calls);
 /* Name of stage i of moe_stage_times, or NULL past the last stage. */

@@ -355,7 +355,12 @@ __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_ma
 
 // ---------------------------------------------------------------------------
 // small numeric helpers
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// SiLU(z) = z * sigmoid(z) = z / (1 + e^-z), with CUDA's fast exponential and
+// fast division intrinsics: the result is rounded to bf16 (or summed into fp32
+// partials of that size) right after, far coarser than their error, and the
+// W1/W3 epilogue runs ~2% faster than with an IEEE division.  For z below
+// about -87 the denominator exceeds 2^126 and the quotient is 0, SiLU's limit.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

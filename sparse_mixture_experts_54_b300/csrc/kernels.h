@@ -138,44 +138,6 @@ cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R,
 cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
                                   int T, int K, int d, const void* resid, void* y, cudaStream_t s);
 
-// the whole small-batch layer in one cooperative persistent kernel
-// (decode_fused.cu): routing, dispatch, gather, W1/W3 and W2 weight streaming,
-// SwiGLU and combine, with grid-wide barriers between the steps.  bar holds
-// fused_decode_bar_ints() ints that must be zero before the first call; every
-// complete call leaves them as it found them.  rstd non-null: RMSNorm the rows
-// first (the residual block; resid then is the residual, usually x == y).
-struct FusedDecodeInput {
-    const __nv_bfloat16* x;
-    const float* Wg;
-    const float* bias;
-    const __nv_bfloat16* resid;
-    __nv_bfloat16* y;
-    int T, d, F, n, K;
-    float norm_eps;
-    int32_t* topk_idx;
-    float* topk_w;
-    float* rstd;
-    int* sched;
-    int32_t* perm;
-    int32_t* inv;
-    __nv_bfloat16* Xp;
-    __nv_bfloat16* H;
-    float* Pa;
-    float* Pb;
-    float* P2;
-    int* bar;
-    KStatus st;
-};
-int fused_decode_bar_ints();
-bool fused_decode_supported(int T, int d, int F, int n, int K, int num_sms);
-// Sets the kernel's shared-memory limit and checks that one CTA per SM fits
-// (cudaErrorNotSupported otherwise); no launch.
-cudaError_t prepare_decode_fused(const FusedDecodeInput& in, int num_sms);
-// mW1/mW3/mW2: 128-row boxes of the weights; mXp32/mH32: 32-row boxes of Xp and H
-cudaError_t launch_decode_fused(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUtensorMap& mW2,
-                                const CUtensorMap& mXp32, const CUtensorMap& mH32, const FusedDecodeInput& in,
-                                int num_sms, cudaStream_t s);
-
 // the same with e4m3 weights and fp32 row scales (decode_fp8.cu); the weight
 // maps come from encode_map_u8_sw64, the partial sums feed launch_decode_swiglu /
 // launch_decode_combine unchanged

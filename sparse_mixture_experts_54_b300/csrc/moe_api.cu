@@ -23,7 +23,6 @@ struct moe_ctx {
     int gemm_pair = 0;          // 0 auto, 1 single CTA, 2 CTA pairs
     int host_out = 1;           // moe_forward_host: 1 = kernels write y into pinned host memory directly
     int fp8_widen = 0;          // moe_forward_fp8: 0 = e4m3 MMA on split token rows, 1 = weights widened to bf16
-    int decode_fused = 0;       // bf16 weight streaming: 1 = the one-kernel path (decode_fused.cu), 0 = five kernels
     int device = 0;
     int num_sms = 148;
     int* status_host = nullptr;   // host-mapped
@@ -39,7 +38,6 @@ struct moe_ctx {
     int32_t* inv = nullptr;
     int* sched = nullptr;
     int* xchg = nullptr;        // grid-barrier words and block counts of the fused routing kernel
-    int* fbar = nullptr;        // grid-barrier words of the one-kernel decode path
     int* ccnt = nullptr;        // [T][d/128] arrival counters of the combine fused into the W2 epilogue
     float* rstd = nullptr;      // [T] 1/rms of each row (residual blocks: RMSNorm before routing)
     void* Xp = nullptr;
@@ -65,7 +63,7 @@ struct moe_ctx {
     // per-stage CUDA-event timing (MOE_OPT_STAGE_TIMING)
     bool stage_timing = false;
     std::vector<cudaEvent_t> ev_free;
-    std::vector<std::array<cudaEvent_t, 6>> ev_calls;
+    std::vector<std::array<cudaEvent_t, 5>> ev_calls;
 };
 
 namespace {
@@ -74,8 +72,8 @@ size_t esize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t topk_idx, topk_w, perm, inv, sched, xchg, fbar, ccnt, rstd, Xp, H, Ys, xbuf, xbuf2, ybuf, Pa, Pb, P2, Xq,
-        Hq, xinv, hinv, total;
+    size_t topk_idx, topk_w, perm, inv, sched, xchg, ccnt, rstd, Xp, H, Ys, xbuf, xbuf2, ybuf, Pa, Pb, P2, Xq, Hq, xinv,
+        hinv, total;
 };
 
 Layout layout_for(const moe_ctx* c, int T, int Tdec) {
@@ -91,7 +89,6 @@ Layout layout_for(const moe_ctx* c, int T, int Tdec) {
     L.inv = take(R * 4);
     L.sched = take(static_cast<size_t>(sched_ints(c->n)) * 4);
     L.xchg = take(static_cast<size_t>(fused_route_xchg_ints()) * 4);
-    L.fbar = take(static_cast<size_t>(fused_decode_bar_ints()) * 4);
     L.ccnt = take(Tn * static_cast<size_t>((c->d + 127) / 128) * 4);
     L.rstd = take(Tn * 4);
     L.Xp = take(R * c->d * es);
@@ -165,7 +162,6 @@ int ensure_workspace(moe_ctx* c, int T, cudaStream_t s, bool decode = false) {
     c->inv = reinterpret_cast<int32_t*>(b + L.inv);
     c->sched = reinterpret_cast<int*>(b + L.sched);
     c->xchg = reinterpret_cast<int*>(b + L.xchg);
-    c->fbar = reinterpret_cast<int*>(b + L.fbar);
     c->ccnt = reinterpret_cast<int*>(b + L.ccnt);
     c->rstd = reinterpret_cast<float*>(b + L.rstd);
     c->Xp = b + L.Xp;
@@ -241,16 +237,13 @@ bool use_decode(const moe_ctx* c, int T) {
 bool use_pair13(const moe_ctx* c) { return c->gemm_pair == 2 && pair_gemm_available(c->num_sms); }
 bool use_pair2(const moe_ctx* c) { return c->gemm_pair != 1 && pair_gemm_available(c->num_sms); }
 
-// Stages of one forward call, in launch order.  The five-kernel and grouped
-// paths run stages 0-3; the one-kernel decode path runs stage 4 alone.
-constexpr int kStages = 5;
-const char* const kStageNames[kStages] = {"route", "expert_w1w3_swiglu", "expert_w2_gate", "combine",
-                                          "decode_fused"};
+// Stages of one forward call, in launch order.
+constexpr int kStages = 4;
+const char* const kStageNames[kStages] = {"route", "expert_w1w3_swiglu", "expert_w2_gate", "combine"};
 
 // Stage boundaries of the current call: an NVTX range for the call and, inside
-// it, one per stage that runs, on the host thread that launches them; CUDA
-// events on the call's stream when stage timing is on (stages that do not run
-// get zero-length intervals).
+// it, one per stage, on the host thread that launches them; CUDA events on the
+// call's stream when stage timing is on.
 struct StageMarks {
     moe_ctx* c = nullptr;
     cudaStream_t s = nullptr;
@@ -312,54 +305,6 @@ int run_route(moe_ctx* c, const void* x, const float* Wg, int T, cudaStream_t s,
     return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
-// The one-kernel decode path (decode_fused.cu): everything of the layer in one
-// cooperative launch.  Returns MOE_ERR_UNSUPPORTED (nothing launched) when the
-// device cannot hold the grid, so that the caller can run the five kernels.
-int run_decode_fused(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2,
-                     void* y, int T, cudaStream_t s, float norm_eps, const void* resid, StageMarks& marks) {
-    CUtensorMap mW1, mW3, mW2;
-    const uint64_t nF = static_cast<uint64_t>(c->n) * c->F, nd = static_cast<uint64_t>(c->n) * c->d;
-    if (!encode_map_bf16_2d(&mW1, W1, nF, c->d, 128) || !encode_map_bf16_2d(&mW3, W3, nF, c->d, 128) ||
-        !encode_map_bf16_2d(&mW2, W2, nd, c->F, 128))
-        return MOE_ERR_CUDA;
-    FusedDecodeInput in{};
-    in.x = static_cast<const __nv_bfloat16*>(x);
-    in.Wg = Wg;
-    in.bias = c->bias;
-    in.resid = static_cast<const __nv_bfloat16*>(resid);
-    in.y = static_cast<__nv_bfloat16*>(y);
-    in.T = T;
-    in.d = c->d;
-    in.F = c->F;
-    in.n = c->n;
-    in.K = c->k;
-    in.norm_eps = norm_eps;
-    in.topk_idx = c->topk_idx;
-    in.topk_w = c->topk_w;
-    in.rstd = norm_eps >= 0.0f ? c->rstd : nullptr;
-    in.sched = c->sched;
-    in.perm = c->perm;
-    in.inv = c->inv;
-    in.Xp = static_cast<__nv_bfloat16*>(c->Xp);
-    in.H = static_cast<__nv_bfloat16*>(c->H);
-    in.Pa = c->Pa;
-    in.Pb = c->Pb;
-    in.P2 = c->P2;
-    in.bar = c->fbar;
-    in.st = kstatus(c);
-    cudaError_t e = prepare_decode_fused(in, c->num_sms);
-    if (e == cudaErrorNotSupported) {
-        cudaGetLastError();
-        return MOE_ERR_UNSUPPORTED;
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
-    marks.begin(kStages - 1);
-    e = launch_decode_fused(mW1, mW3, mW2, c->map_Xp32, c->map_H32, in, c->num_sms, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    marks.finish();
-    return MOE_OK;
-}
-
 // y = MoE(x); with norm_eps >= 0 and resid: y = resid + MoE(RMSNorm(x)) (the
 // residual block of a stack, x == resid == y allowed).
 int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, const void* W3, const void* W2, void* y,
@@ -367,11 +312,6 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
     const ElemType et = c->dtype == MOE_F32 ? ElemType::F32 : ElemType::BF16;
     const int R = c->k * T;
     StageMarks marks(c, s);
-    if (et == ElemType::BF16 && use_decode(c, T) && c->decode_fused &&
-        fused_decode_supported(T, c->d, c->F, c->n, c->k, c->num_sms)) {
-        const int rc = run_decode_fused(c, x, Wg, W1, W3, W2, y, T, s, norm_eps, resid, marks);
-        if (rc != MOE_ERR_UNSUPPORTED) return rc;
-    }
     marks.begin(0);
     int rc = run_route(c, x, Wg, T, s, nullptr, true, norm_eps);
     if (rc != MOE_OK) return rc;
@@ -600,10 +540,6 @@ int moe_set_option(moe_ctx* c, int option, long long value) {
         case MOE_OPT_FP8_WIDEN:
             if (value < 0 || value > 1) return MOE_ERR_INVALID;
             c->fp8_widen = static_cast<int>(value);
-            return MOE_OK;
-        case MOE_OPT_DECODE_FUSED:
-            if (value < 0 || value > 1) return MOE_ERR_INVALID;
-            c->decode_fused = static_cast<int>(value);
             return MOE_OK;
         default:
             return MOE_ERR_INVALID;

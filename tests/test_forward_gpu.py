@@ -359,105 +359,3 @@ def test_decode_and_grouped_paths_agree_and_are_deterministic():
     _, y_grp, _, _ = run_layer(w, layer, path=1)
     assert torch.equal(y_dec, y_dec2)
     assert_close(y_to_numpy(y_dec), y_to_numpy(y_grp), "bf16")
-
-
-# ----------------------------------------------------------------------------- one-kernel decode path
-FUSED_CASES = [
-    # T, d, F, n, K, bias
-    (1, 256, 256, 8, 2, None),
-    (5, 512, 384, 8, 2, None),
-    (32, 256, 256, 8, 2, (0, 0, 1.5, 0, 0, 0.5, 0, 0)),
-    (77, 256, 384, 8, 3, None),
-    (120, 768, 640, 16, 2, None),
-    (100, 256, 256, 4, 1, None),
-    (16, 256, 256, 8, 8, None),
-    (140, 512, 384, 20, 2, None),
-    (148, 256, 256, 8, 2, None),
-]
-
-
-@pytest.mark.parametrize("T,d,F,n,K,bias", FUSED_CASES)
-def test_fused_decode_equals_the_five_kernels_bitwise(T, d, F, n, K, bias):
-    """The one-kernel decode path routes with the routing kernel's arithmetic,
-    splits K the same way and sums in the same orders, so its output equals the
-    five-kernel path's bit for bit; both are checked against the oracle."""
-    w = inputs.Workload("fused", T=T, d=d, d_ff=F, n_experts=n, k=K, bias=bias, seed=500 + T + d)
-    layer = inputs.make_layer(w, "cuda")
-    ys = {}
-    for fused in (1, 0):
-        m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=layer["bias"])
-        m.set_option(_lib.MOE_OPT_FORCE_PATH, 2)
-        m.set_option(_lib.MOE_OPT_DECODE_FUSED, fused)
-        ys[fused] = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
-        torch.cuda.synchronize()
-        assert m.status() == 0, _lib.moe_error_string(m.status())
-        if fused:
-            r = m.route(layer["x"], layer["Wg"])
-            gidx, gw = r["topk_idx"].cpu().numpy(), r["topk_w"].cpu().numpy()
-        m.close()
-    assert torch.equal(ys[1], ys[0])
-    y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
-    check_route(gidx, gw, ref["logits"], ref["idx"], ref["gate"], K)
-    assert_close(y_to_numpy(ys[1]), y_ref, "bf16")
-
-
-@pytest.mark.parametrize("T", [1, 8, 64])
-def test_fused_decode_residual_block_equals_the_five_kernels(T):
-    # h <- h + MoE(RMSNorm(h)) in place: the one-kernel path normalises in its
-    # routing step and adds the residual in its combine step
-    w = inputs.Workload("fused_blk", T=T, d=512, d_ff=384, seed=600 + T)
-    layer = inputs.make_layer(w, "cuda")
-    h0 = (layer["x"].float() * 3.0).to(torch.bfloat16)
-    hs = {}
-    for fused in (1, 0):
-        m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
-        m.set_option(_lib.MOE_OPT_DECODE_FUSED, fused)
-        h = h0.clone()
-        for _ in range(3):   # three blocks in a row on the same weights
-            m.block_forward(h, layer["Wg"], layer["W1"], layer["W3"], layer["W2"], 1e-5)
-        torch.cuda.synchronize()
-        assert m.status() == 0
-        hs[fused] = h
-        m.close()
-    assert torch.equal(hs[1], hs[0])
-
-
-@pytest.mark.parametrize("T", [1, 32, 128])
-def test_mixtral_fused_decode_equals_the_five_kernels(decode_cases, T):
-    # at d = 4096 the router's fp32 sums run over sixteen row segments, so this
-    # also checks that the one-kernel path routes with the routing kernel's order
-    case = decode_cases(T)
-    layer = dict(x=case.x, Wg=case.Wg, bias=case.b, W1=case.W1, W3=case.W3, W2=case.W2)
-    ys = {}
-    for fused in (1, 0):
-        m = MoELayer(case.w.d, case.w.d_ff, case.w.n_experts, case.w.k, bias=case.b)
-        m.set_option(_lib.MOE_OPT_DECODE_FUSED, fused)
-        ys[fused] = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
-        torch.cuda.synchronize()
-        assert m.status() == 0
-        m.close()
-    assert torch.equal(ys[1], ys[0])
-
-
-def test_fused_decode_replays_from_a_cuda_graph():
-    # the grid-barrier words return to zero after every call, so a captured call
-    # replays; each replay equals an eager call on the same input bit for bit
-    w = inputs.Workload("fused_graph", T=24, d=512, d_ff=384, seed=31)
-    layer = inputs.make_layer(w, "cuda")
-    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
-    m.set_option(_lib.MOE_OPT_DECODE_FUSED, 1)
-    m.reserve(w.T)
-    args = (layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
-    x = layer["x"].clone()
-    y = torch.empty_like(x)
-    m.forward(x, *args, y=y)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        m.forward(x, *args, y=y)
-    for i in range(3):
-        x.copy_(inputs.make_x(w, "cuda", seed=400 + i))
-        g.replay()
-        torch.cuda.synchronize()
-        assert torch.equal(y, m.forward(x, *args)), f"replay {i}"
-    assert m.status() == 0

@@ -3,11 +3,10 @@
 A profiler that records NVTX attaches to a process through the variable
 NVTX_INJECTION64_PATH: the first NVTX call loads the named library and lets it
 fill the range functions.  This test builds such a library (a few lines of C
-that log pushes and pops to a file), runs moe_forward on each of its paths and
-one moe_forward_fp8 call in a child process with it attached, and checks the
-nesting: one range per call holding one range per stage that ran, named as the
-stages of moe_stage_times (the one-kernel decode path is the single stage
-"decode_fused").
+that log pushes and pops to a file), runs moe_forward on its grouped path,
+moe_block_forward on its weight-streaming path and one moe_forward_fp8 call in
+a child process with it attached, and checks the nesting: one range per call
+holding one range per stage, named as the stages of moe_stage_times.
 """
 import os
 import subprocess
@@ -55,10 +54,7 @@ CHILD = textwrap.dedent("""
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k)
     m.forward(layer["x"], *args)                    # grouped GEMMs
     h = x40.clone()
-    m.set_option(_lib.MOE_OPT_DECODE_FUSED, 1)
-    m.block_forward(h, *args, 1e-5)                 # one-kernel decode path
-    m.set_option(_lib.MOE_OPT_DECODE_FUSED, 0)
-    m.forward(x40, *args)                           # five decode kernels
+    m.block_forward(h, *args, 1e-5)                 # weight-streaming kernels, residual block
     q = [inputs.quantize_e4m3_rows(layer[n]) for n in ("W1", "W3", "W2")]
     m.forward_fp8(x40, layer["Wg"], q[0][0], q[0][1], q[1][0], q[1][1], q[2][0], q[2][1])
     torch.cuda.synchronize()
@@ -95,8 +91,7 @@ def test_forward_calls_emit_one_nvtx_range_per_stage(tmp_path):
     assert out.returncode == 0, out.stdout + out.stderr
     calls = parse(log.read_text().split("\n"))
     stages = ["route", "expert_w1w3_swiglu", "expert_w2_gate", "combine"]
-    assert [c[0] for c in calls] == ["moe_forward", "moe_forward", "moe_forward", "moe_forward_fp8"]
-    expect = [stages, ["decode_fused"], stages, stages]
-    for (name, children), want in zip(calls, expect):
-        assert [c[0] for c in children] == want, (name, children)
+    assert [c[0] for c in calls] == ["moe_forward", "moe_forward", "moe_forward_fp8"]
+    for name, children in calls:
+        assert [c[0] for c in children] == stages, (name, children)
         assert all(not c[1] for c in children)
