@@ -65,6 +65,10 @@ def w13_traffic():
     return int(t["dram_bytes_per_launch"]), t.get("command", "")
 
 
+# Headline windows up to this long are timed against the burst GEMM peak.
+BURST_WINDOW_MS = 250.0
+
+
 def peaks():
     p = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -343,11 +347,20 @@ def run_ours(args, rank, world, dist):
     k13_ms = ms_p * share
     achieved = alg_p["flops_w13"] / (k13_ms * 1e-3) / 1e12
     traffic, traffic_note = w13_traffic()
+    # The peak that fits the window: the burst GEMM rate for a window of a few tens
+    # of calls (clocks near their maximum), the sustained one for a window long
+    # enough to reach the power-capped steady state.
+    window_ms = ms_p * args.steps
+    kind = "burst" if window_ms <= BURST_WINDOW_MS else "sustained"
+    peak = pk["bf16_tflops"] if kind == "burst" else pk["bf16_tflops_sustained"]
     roofline = {"kernel": "expert_w1w3_swiglu (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
-                "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / pk["bf16_tflops"], 4),
-                "peak_kind": f"bf16 burst ({pk['source']}): the headline window is {args.steps} calls, "
-                             f"{ms_p * args.steps:.0f} ms",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "peak_kind": f"bf16 {kind} ({pk['source']}): the headline window is {args.steps} calls, "
+                             f"{window_ms:.0f} ms ({'at most' if kind == 'burst' else 'over'} "
+                             f"{BURST_WINDOW_MS:.0f} ms)",
+                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4),
+                "frac_of_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
                 "frac_of_nominal_2250": round(achieved / 2250.0, 4),
                 "flops_per_launch": alg_p["flops_w13"],
                 "duration_us": round(k13_ms * 1e3, 1),
