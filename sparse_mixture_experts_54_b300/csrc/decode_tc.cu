@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(256, 2) decode_swiglu_kernel(const float4* __r
     griddep_wait();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < part4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const float4 a = sum_splits(Pa + i, part4, S), b = sum_splits(Pb + i, part4, S);
+        float4 a, b;
+        sum_splits_pair(Pa + i, Pb + i, part4, S, a, b);
         uint2 o;
         o.x = pack_bf16x2(silu_f(a.x) * b.x, silu_f(a.y) * b.y);
         o.y = pack_bf16x2(silu_f(a.z) * b.z, silu_f(a.w) * b.w);
@@ -306,9 +307,13 @@ __global__ void __launch_bounds__(256, 2) decode_swiglu_kernel(const float4* __r
 }
 
 // y[t][i] = sum_k g[t][k] * (sum_s P2[s][inv[t*K+k]][i]), slots in order, one rounding.
-// With resid (may be y itself): y = resid + that sum, one rounding.
-template <typename TY>
-__global__ void __launch_bounds__(256, 2) decode_combine_kernel(const float4* __restrict__ P2, int S, size_t part4,
+// With resid (may be y itself): y = resid + that sum, one rounding.  PAIR (K = 2,
+// small batches): both slot rows' split loads go out together, one round trip
+// to L2 per 8 splits instead of two; the registers that takes allow one block
+// per SM, which the few blocks of a small batch do not miss.  Same arithmetic
+// in the same order either way.
+template <typename TY, bool PAIR>
+__global__ void __launch_bounds__(256, PAIR ? 1 : 2) decode_combine_kernel(const float4* __restrict__ P2, int S, size_t part4,
                                                              const int32_t* __restrict__ inv,
                                                              const float* __restrict__ topk_w, int T, int K, int d4,
                                                              const TY* resid, TY* y) {
@@ -319,12 +324,24 @@ __global__ void __launch_bounds__(256, 2) decode_combine_kernel(const float4* __
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const size_t t = i / d4, c = i % d4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < K; ++k) {
-            const size_t a = t * K + k;
-            const size_t row = static_cast<size_t>(inv[a]);
-            const float g = topk_w[a];
-            const float4 v = sum_splits(P2 + row * d4 + c, part4, S);
-            acc.x += g * v.x; acc.y += g * v.y; acc.z += g * v.z; acc.w += g * v.w;
+        if (PAIR) {
+            const size_t row0 = static_cast<size_t>(inv[2 * t]), row1 = static_cast<size_t>(inv[2 * t + 1]);
+            const float g0 = topk_w[2 * t], g1 = topk_w[2 * t + 1];
+            float4 v0, v1;
+            sum_splits_pair(P2 + row0 * d4 + c, P2 + row1 * d4 + c, part4, S, v0, v1);
+            acc.x = fmaf(g0, v0.x, acc.x); acc.y = fmaf(g0, v0.y, acc.y);
+            acc.z = fmaf(g0, v0.z, acc.z); acc.w = fmaf(g0, v0.w, acc.w);
+            acc.x = fmaf(g1, v1.x, acc.x); acc.y = fmaf(g1, v1.y, acc.y);
+            acc.z = fmaf(g1, v1.z, acc.z); acc.w = fmaf(g1, v1.w, acc.w);
+        } else {
+            for (int k = 0; k < K; ++k) {
+                const size_t a = t * K + k;
+                const size_t row = static_cast<size_t>(inv[a]);
+                const float g = topk_w[a];
+                const float4 v = sum_splits(P2 + row * d4 + c, part4, S);
+                acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
+                acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
+            }
         }
         if (resid) {
             float r[4];
@@ -455,12 +472,16 @@ cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, co
     int blocks = static_cast<int>((total + 255) / 256);
     if (blocks > 148 * 8) blocks = 148 * 8;
     if (blocks < 1) blocks = 1;
-    if (et == ElemType::BF16)
-        return launch_pdl(decode_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
-                          reinterpret_cast<const float4*>(P2), S, part4, inv, topk_w, T, K, d4,
-                          static_cast<const __nv_bfloat16*>(resid), static_cast<__nv_bfloat16*>(y));
-    return launch_pdl(decode_combine_kernel<float>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2),
-                      S, part4, inv, topk_w, T, K, d4, static_cast<const float*>(resid), static_cast<float*>(y));
+    // the pair kernel while its threads fit in one wave of one block per SM
+    const bool pair = K == 2 && blocks <= 148;
+    if (et == ElemType::BF16) {
+        auto kern = pair ? decode_combine_kernel<__nv_bfloat16, true> : decode_combine_kernel<__nv_bfloat16, false>;
+        return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2), S, part4, inv,
+                          topk_w, T, K, d4, static_cast<const __nv_bfloat16*>(resid), static_cast<__nv_bfloat16*>(y));
+    }
+    auto kern = pair ? decode_combine_kernel<float, true> : decode_combine_kernel<float, false>;
+    return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2), S, part4, inv, topk_w,
+                      T, K, d4, static_cast<const float*>(resid), static_cast<float*>(y));
 }
 
 }  // namespace moe

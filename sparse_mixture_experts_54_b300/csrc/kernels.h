@@ -127,6 +127,31 @@ __device__ __forceinline__ float4 sum_splits(const float4* __restrict__ p, size_
     return a;
 }
 
+// Two such sums at once, their loads issued together (each still in s order).
+__device__ __forceinline__ void sum_splits_pair(const float4* __restrict__ p, const float4* __restrict__ q,
+                                                size_t stride, int S, float4& a, float4& b) {
+    a = b = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        float4 u[8], v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < S) {
+                u[j] = __ldg(p + static_cast<size_t>(s0 + j) * stride);
+                v[j] = __ldg(q + static_cast<size_t>(s0 + j) * stride);
+            }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j == 0) {
+                a = u[0];
+                b = v[0];
+            } else if (s0 + j < S) {
+                a.x += u[j].x; a.y += u[j].y; a.z += u[j].z; a.w += u[j].w;
+                b.x += v[j].x; b.y += v[j].y; b.z += v[j].z; b.w += v[j].w;
+            }
+        }
+    }
+}
+
 int decode_pick_splits(int units, int kblocks, int num_sms);
 cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
                               const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,

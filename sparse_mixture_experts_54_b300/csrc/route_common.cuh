@@ -38,7 +38,7 @@ __device__ __forceinline__ void load8(const TX* row, int j0, int d, float (&v)[8
 template <int NMAX>
 __device__ __forceinline__ void topk_gate_write(const float (&l)[NMAX], int n, int K, int t, int lane,
                                                 int32_t* topk_idx, float* topk_w, float* logits_out,
-                                                int* hist = nullptr) {
+                                                int* hist = nullptr, int* local_idx = nullptr) {
     float mine = 0.0f, lmax = -INFINITY;
 #pragma unroll
     for (int e = 0; e < NMAX; ++e) {
@@ -61,6 +61,7 @@ __device__ __forceinline__ void topk_gate_write(const float (&l)[NMAX], int n, i
         topk_idx[static_cast<size_t>(t) * K + rank] = lane;
         topk_w[static_cast<size_t>(t) * K + rank] = num / z;
         if (hist) atomicAdd(hist + lane, 1);   // a count: the order of the adds does not matter
+        if (local_idx) local_idx[rank] = lane;  // the same choice, for a caller that reads it back soon
     }
     if (logits_out && lane < n) logits_out[static_cast<size_t>(t) * n + lane] = mine;
 }

@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     __shared__ int wtab[FR_WARPS][33];
     __shared__ int s_ok;
     __shared__ float s_ss[FR_TG * TOKW][FR_DS];   // NORM: quarter sums of squares
+    __shared__ int s_topk[32];                    // SMALL: the block's token's K experts, in rank order
     constexpr int TPB = FR_TG * TOKW;   // tokens per block iteration
     constexpr int V = TOKW * NMAX;
 
@@ -121,6 +122,22 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
             }
         }
     }
+    // SMALL: W_g is read from L2 in the loop below; with up to 8 experts this
+    // warp's first segment of it is loaded here, before the wait, so that only
+    // x's loads follow it (64 registers; more experts would spill).
+    constexpr bool WPRE = SMALL && NMAX <= 8;
+    float4 wpre[WPRE ? NMAX : 1][2];
+    if constexpr (WPRE) {
+        const int j0 = (warp % FR_DS) * 256 + 4 * lane, j1 = j0 + 128;
+#pragma unroll
+        for (int e = 0; e < NMAX; ++e) {
+            wpre[e][0] = wpre[e][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < p.n) {
+                if (j0 < p.d) wpre[e][0] = __ldg(reinterpret_cast<const float4*>(p.Wg + static_cast<size_t>(e) * p.d + j0));
+                if (j1 < p.d) wpre[e][1] = __ldg(reinterpret_cast<const float4*>(p.Wg + static_cast<size_t>(e) * p.d + j1));
+            }
+        }
+    }
     if (tid < 32) s_hist[tid] = 0;
     griddep_wait();
     __syncthreads();
@@ -130,6 +147,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     const int t_end = min(p.T, t_begin + p.chunk);
     const TX* x = static_cast<const TX*>(p.x);
     const int tg = warp / FR_DS, q = warp % FR_DS;
+    float rs_small = 1.0f;   // SMALL + NORM: the block's token's 1/rms, for the gather
     for (int tb = t_begin; tb < t_end; tb += TPB) {
         float acc[TOKW][NMAX];
 #pragma unroll
@@ -177,6 +195,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
                 rs[j] = 1.0f / sqrtf(tot / static_cast<float>(d) + p.norm_eps);
                 if (q == 0 && lane == 0 && t0 + j < t_end) p.rstd[t0 + j] = rs[j];
             }
+            if (SMALL) rs_small = rs[0];
         }
         // x of the first segment; inside the loop the next segment's loads are
         // issued before the current one is used
@@ -216,8 +235,13 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
                     const float* w = wg_s + static_cast<size_t>(e) * d;
                     float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;
                     if (SMALL) {
-                        if (h0) w0 = __ldg(reinterpret_cast<const float4*>(w + j0));
-                        if (h1) w1 = __ldg(reinterpret_cast<const float4*>(w + j1));
+                        if (WPRE && sg == q) {
+                            w0 = wpre[WPRE ? e : 0][0];
+                            w1 = wpre[WPRE ? e : 0][1];
+                        } else {
+                            if (h0) w0 = __ldg(reinterpret_cast<const float4*>(w + j0));
+                            if (h1) w1 = __ldg(reinterpret_cast<const float4*>(w + j1));
+                        }
                     } else {
                         if (h0) w0 = *reinterpret_cast<const float4*>(w + j0);
                         if (h1) w1 = *reinterpret_cast<const float4*>(w + j1);
@@ -260,19 +284,23 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
                     }
                     l[e] = s;
                 }
-                topk_gate_write<NMAX>(l, n, K, t, lane, p.topk_idx, p.topk_w, p.logits, s_hist);
+                topk_gate_write<NMAX>(l, n, K, t, lane, p.topk_idx, p.topk_w, p.logits, s_hist,
+                                      SMALL ? s_topk : nullptr);
             }
         }
         __syncthreads();
     }
 
     // ---------------- grid barrier: publish and collect the block counts ----------------
+    // (one block: nothing to exchange; its own counts are the totals)
     int* cnt_word = p.xchg;
     int* gen_word = p.xchg + 1;
     int* bcounts = p.xchg + 2;
-    if (tid < 32) bcounts[b * 32 + tid] = tid < n ? s_hist[tid] : 0;
+    if (G > 1 && tid < 32) bcounts[b * 32 + tid] = tid < n ? s_hist[tid] : 0;
     __syncthreads();
-    if (tid == 0) {
+    if (G == 1) {
+        if (tid == 0) s_ok = 1;
+    } else if (tid == 0) {
         const int g = ld_acquire_gpu(gen_word);
         __threadfence();
         const int prev = atomicAdd(cnt_word, 1);
@@ -308,10 +336,14 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     // the order does not matter).
     for (int e = warp; e < n; e += FR_WARPS) {
         int tot = 0, pre = 0;
-        for (int bb = lane; bb < G; bb += 32) {
-            const int c = __ldcg(bcounts + bb * 32 + e);
-            tot += c;
-            pre += bb < b ? c : 0;
+        if (G == 1) {
+            tot = lane == 0 ? s_hist[e] : 0;
+        } else {
+            for (int bb = lane; bb < G; bb += 32) {
+                const int c = __ldcg(bcounts + bb * 32 + e);
+                tot += c;
+                pre += bb < b ? c : 0;
+            }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -353,7 +385,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     const int R = p.T * K;
     for (int a0 = a_begin; a0 < a_end; a0 += FR_ROUND) {
         const int a = a0 + tid;
-        int e = a < a_end ? p.topk_idx[a] : -1;   // this block's own phase-1 writes
+        int e = a < a_end ? (SMALL ? s_topk[a - a_begin] : p.topk_idx[a]) : -1;   // this block's phase-1 choices
         // Index checks on every placement (one compare each): an expert id
         // outside [0, n) or a position outside [0, K*T) is never used as an
         // address; the call records MOE_ERR_BOUNDS in the status word instead.
@@ -407,7 +439,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
                 const uint4* src = xv4 + static_cast<size_t>(t) * rv;
                 uint4* dst = xp4 + static_cast<size_t>(ap.y) * rv;
                 float rsv = 1.0f;
-                if constexpr (NORM) rsv = p.rstd[t];   // written by this block in phase 1
+                if constexpr (NORM) rsv = SMALL ? rs_small : p.rstd[t];   // this block's phase-1 value
                 for (int v0 = lane; v0 < rv; v0 += 32 * 16) {
                     uint4 buf[16];
 #pragma unroll
