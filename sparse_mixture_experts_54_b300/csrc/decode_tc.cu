@@ -23,6 +23,7 @@
 // accumulator sets in flight so the copy-out overlaps the next item.  Every
 // wait is bounded, as in gemm_tc.cu.
 #include "kernels.h"
+#include "route_common.cuh"
 
 namespace moe {
 
@@ -55,12 +56,16 @@ struct DecArgs {
     float* Pb;            // [S][R][ld] (MODE 0 only)
     int R;
     int ld;               // output features (F for MODE 0, d for MODE 1)
+    // Schedule-ready word (may be null): the routing kernel clears it, MODE 0
+    // sets it once it holds the call's schedule, MODE 1 reads it to start its
+    // weight loads before the wait on the kernel before it.
+    int* ready;
     KStatus st;
 };
 
 static size_t decode_smem_bytes(int stages, int stage_bytes) {
     return 1024 + static_cast<size_t>(stages) * stage_bytes + D_NUM_BARS * 8 + 16 + (3 * D_MAX_EXPERTS + 2) * 4 +
-           D_MAX_EXPERTS * 4;
+           D_MAX_EXPERTS * 4 + 16;
 }
 
 template <int MODE>
@@ -77,6 +82,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_sched = reinterpret_cast<int*>(tmem_slot + 4);
     int* s_touched = s_sched + 3 * D_MAX_EXPERTS + 2;   // touched experts, in expert order
+    int* s_early = s_touched + D_MAX_EXPERTS;           // MODE 1: schedule known before the wait
 
     const uint32_t bar0 = smem_u32(bars);
     const int S = p.stages;
@@ -113,11 +119,31 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     }
     // Everything above touches no buffer of the layer; the schedule and the
     // token rows come from the kernels before this one.
-    griddep_wait();
-    for (int i = threadIdx.x; i < 3 * n + 2; i += D_THREADS) s_sched[i] = p.sched[i];
+    //
+    // W2 (MODE 1) reads H, which the SwiGLU kernel right before it writes, but its
+    // weights and schedule are older: the W1/W3 kernel of the same call has set the
+    // ready word (release) after its own wait on the routing kernel.  When the word
+    // is set, this kernel reads the schedule at once and its producer sends the
+    // first ring's worth of weight tiles before waiting for the SwiGLU kernel; only
+    // the token rows (H) and everything after wait.  The routing kernel of every
+    // call clears the word once the previous call has finished, so a set word is
+    // always this call's.
+    bool early = false;
+    if (MODE == 1 && p.ready) {
+        if (threadIdx.x == 0) {
+            int v = 0;
+            for (int i = 0; i < 64 && v == 0; ++i) v = ld_acquire_gpu(p.ready);
+            *s_early = v;
+        }
+        __syncthreads();
+        early = *s_early != 0;
+    }
+    if (!early) griddep_wait();
+    for (int i = threadIdx.x; i < 3 * n + 2; i += D_THREADS) s_sched[i] = __ldcg(p.sched + i);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (MODE == 0 && p.ready && blockIdx.x == 0 && threadIdx.x == 0) st_release_gpu(p.ready, 1);
     if (threadIdx.x == 0) {
         int nt = 0;
         for (int e = 0; e < n; ++e)
@@ -154,6 +180,24 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // early (MODE 1): the first `pre` stages (first use of the ring, no
+            // empty wait) get their byte count and weight tile now; their token
+            // rows follow the wait, in the loop below
+            int pre = 0;
+            if (early) {
+                for (int it = blockIdx.x; it < items && pre < S; it += gridDim.x) {
+                    int e, rb, sp;
+                    decode_item(it, e, rb, sp);
+                    const int nbox = item_n(e) / D_B_BOX;
+                    const int arow = e * p.rows_per_e + rb * 128;
+                    const uint32_t bytes = A_TILES * D_A_BYTES + nbox * D_B_BOX * D_BK * 2;
+                    for (int kb = sp * p.kb_per_split; kb < (sp + 1) * p.kb_per_split && pre < S; ++kb, ++pre) {
+                        mbar_arrive_expect_tx(full_bar(pre), bytes);
+                        tma_load_2d(ring_u32 + pre * p.stage_bytes, &tmA0, full_bar(pre), kb * D_BK, arow, pol_w);
+                    }
+                }
+                griddep_wait();
+            }
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
                 int e, rb, sp;
                 decode_item(it, e, rb, sp);
@@ -162,12 +206,14 @@ __global__ void __launch_bounds__(D_THREADS, 1)
                 const int brow = offsets[e];
                 const uint32_t bytes = A_TILES * D_A_BYTES + nbox * D_B_BOX * D_BK * 2;
                 for (int kb = sp * p.kb_per_split; kb < (sp + 1) * p.kb_per_split; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
                     const uint32_t a_dst = ring_u32 + stage * p.stage_bytes;
                     const uint32_t b_dst = a_dst + A_TILES * D_A_BYTES;
-                    mbar_arrive_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(a_dst, &tmA0, full_bar(stage), kb * D_BK, arow, pol_w);
-                    if (MODE == 0) tma_load_2d(a_dst + D_A_BYTES, &tmA1, full_bar(stage), kb * D_BK, arow, pol_w);
+                    if (issued >= pre) {
+                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, st, abort_flag)) { ok = false; break; }
+                        mbar_arrive_expect_tx(full_bar(stage), bytes);
+                        tma_load_2d(a_dst, &tmA0, full_bar(stage), kb * D_BK, arow, pol_w);
+                        if (MODE == 0) tma_load_2d(a_dst + D_A_BYTES, &tmA1, full_bar(stage), kb * D_BK, arow, pol_w);
+                    }
                     for (int bb = 0; bb < nbox; ++bb)
                         tma_load_2d(b_dst + bb * D_B_BOX * D_BK * 2, &tmB, full_bar(stage), kb * D_BK,
                                     brow + bb * D_B_BOX, pol_x);
@@ -417,9 +463,10 @@ static cudaError_t launch_decode(const CUtensorMap& a0, const CUtensorMap& a1, c
 
 cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
                               const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,
-                              KStatus st, int num_sms, cudaStream_t s) {
+                              KStatus st, int num_sms, cudaStream_t s, int* ready) {
     if (n > D_MAX_EXPERTS - 1 || T <= 0 || T > kDecodeMaxT) return cudaErrorInvalidValue;
     DecArgs args{};
+    args.ready = ready;
     args.sched = sched;
     args.n = n;
     args.row_blocks = F / 128;
@@ -436,9 +483,11 @@ cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3
 }
 
 cudaError_t launch_decode_w2(const CUtensorMap& mapW2, const CUtensorMap& mapH32, const int* sched, int n, int d,
-                             int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s) {
+                             int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s,
+                             int* ready) {
     if (n > D_MAX_EXPERTS - 1 || T <= 0 || T > kDecodeMaxT) return cudaErrorInvalidValue;
     DecArgs args{};
+    args.ready = ready;
     args.sched = sched;
     args.n = n;
     args.row_blocks = d / 128;

@@ -60,10 +60,14 @@ cudaError_t launch_combine(ElemType et, const float* Ys, int T, int K, int d, co
 
 // Router + top-k + dispatch + row gather in one kernel (route_fused.cu).  xchg
 // holds fused_route_xchg_ints() ints that must be zero before the first call;
-// every complete call leaves them as it found them.  Xp and logits may be null.
+// every complete call leaves its barrier words as it found them (the ready word
+// is cleared at the start of every call).  Xp and logits may be null.
 // rstd non-null ([T] floats): RMSNorm the rows first (eps = norm_eps).
 constexpr int kFusedRouteMaxBlocks = 160;
-inline int fused_route_xchg_ints() { return 2 + kFusedRouteMaxBlocks * 32; }
+// The word after the block counts is the schedule-ready word of the decode
+// kernels (cleared by the routing kernel of every call).
+constexpr int kReadyWord = 2 + kFusedRouteMaxBlocks * 32;
+inline int fused_route_xchg_ints() { return kReadyWord + 1; }
 int fused_route_blocks(int T, int num_sms);
 cudaError_t launch_fused_route(ElemType et, const void* x, const float* Wg, const float* bias, int T, int d, int n,
                                int K, int32_t* topk_idx, float* topk_w, float* logits, int* sched, int32_t* perm,
@@ -153,11 +157,15 @@ __device__ __forceinline__ void sum_splits_pair(const float4* __restrict__ p, co
 }
 
 int decode_pick_splits(int units, int kblocks, int num_sms);
+// ready (may be null): the schedule-ready word (xchg + kReadyWord) of the
+// routing kernel that ran first in the call; the W1/W3 kernel sets it and the W2
+// kernel then sends its first weight tiles before waiting on the SwiGLU kernel.
 cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
                               const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,
-                              KStatus st, int num_sms, cudaStream_t s);
+                              KStatus st, int num_sms, cudaStream_t s, int* ready = nullptr);
 cudaError_t launch_decode_w2(const CUtensorMap& mapW2_128, const CUtensorMap& mapH32, const int* sched, int n, int d,
-                             int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s);
+                             int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s,
+                             int* ready = nullptr);
 cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R, int F, __nv_bfloat16* H,
                                  cudaStream_t s);
 cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,

@@ -334,13 +334,15 @@ int run_forward(moe_ctx* c, const void* x, const float* Wg, const void* W1, cons
         const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 64, c->num_sms);
         const int s1 = decode_pick_splits(touched * (c->d / 128), c->F / 64, c->num_sms);
         marks.begin(1);
+        int* ready = c->xchg + kReadyWord;
         e = launch_decode_w13(mW1, mW3, c->map_Xp32, c->sched, c->n, c->d, c->F, T, c->k, s0, c->Pa, c->Pb, st,
-                              c->num_sms, s);
+                              c->num_sms, s, ready);
         if (e != cudaSuccess) return cuda_fail(e);
         e = launch_decode_swiglu(c->Pa, c->Pb, s0, R, c->F, static_cast<__nv_bfloat16*>(c->H), s);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.begin(2);
-        e = launch_decode_w2(mW2, c->map_H32, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms, s);
+        e = launch_decode_w2(mW2, c->map_H32, c->sched, c->n, c->d, c->F, T, c->k, s1, c->P2, st, c->num_sms, s,
+                             ready);
         if (e != cudaSuccess) return cuda_fail(e);
         marks.begin(3);
         e = launch_decode_combine(et, c->P2, s1, R, c->inv, c->topk_w, T, c->k, c->d, resid, y, s);

@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(FR_THREADS, 1) route_fused_kernel(FusedRouteAr
     }
     if (tid < 32) s_hist[tid] = 0;
     griddep_wait();
+    // the previous call has finished: its schedule-ready word goes back to 0
+    if (b == 0 && tid == 0) p.xchg[kReadyWord] = 0;
     __syncthreads();
 
     // ---------------- phase 1: logits, top-k, gates, block counts ----------------
