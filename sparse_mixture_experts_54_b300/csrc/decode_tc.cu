@@ -131,8 +131,10 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     bool early = false;
     if (MODE == 1 && p.ready) {
         if (threadIdx.x == 0) {
-            int v = 0;
-            for (int i = 0; i < 64 && v == 0; ++i) v = ld_acquire_gpu(p.ready);
+            // a few microseconds at most; past that the kernel waits as usual
+            const uint64_t t0 = globaltimer_ns();
+            int v = ld_acquire_gpu(p.ready);
+            while (v == 0 && globaltimer_ns() - t0 < 3000) v = ld_acquire_gpu(p.ready);
             *s_early = v;
         }
         __syncthreads();
