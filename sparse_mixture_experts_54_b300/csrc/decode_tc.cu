@@ -339,14 +339,18 @@ __global__ void __launch_bounds__(D_THREADS, 1)
 
 // ---------------------------------------------------------------------------
 // H[r][f] = bf16( SiLU(sum_s Pa[s][r][f]) * sum_s Pb[s][r][f] ), parts added in order.
-__global__ void __launch_bounds__(256, 2) decode_swiglu_kernel(const float4* __restrict__ Pa, const float4* __restrict__ Pb,
-                                                            int S, size_t part4, uint2* __restrict__ H) {
+// kBatch: splits per round trip; 2 (S <= 2, the larger batches) leaves registers
+// for 4 blocks per SM, so a T = 32 layer's 896 blocks fit in one wave.
+template <int kBatch>
+__global__ void __launch_bounds__(256, kBatch <= 2 ? 4 : 2)
+    decode_swiglu_kernel(const float4* __restrict__ Pa, const float4* __restrict__ Pb, int S, size_t part4,
+                         uint2* __restrict__ H) {
     griddep_launch_dependents();
     griddep_wait();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < part4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         float4 a, b;
-        sum_splits_pair(Pa + i, Pb + i, part4, S, a, b);
+        sum_splits_pair<kBatch>(Pa + i, Pb + i, part4, S, a, b);
         uint2 o;
         o.x = pack_bf16x2(silu_f(a.x) * b.x, silu_f(a.y) * b.y);
         o.y = pack_bf16x2(silu_f(a.z) * b.z, silu_f(a.w) * b.w);
@@ -511,7 +515,8 @@ cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R,
     int blocks = static_cast<int>((part4 + 255) / 256);
     if (blocks > 148 * 8) blocks = 148 * 8;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(decode_swiglu_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(Pa),
+    auto kern = S <= 2 ? decode_swiglu_kernel<2> : decode_swiglu_kernel<8>;
+    return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(Pa),
                       reinterpret_cast<const float4*>(Pb), S, part4, reinterpret_cast<uint2*>(H));
 }
 

@@ -131,20 +131,22 @@ __device__ __forceinline__ float4 sum_splits(const float4* __restrict__ p, size_
     return a;
 }
 
-// Two such sums at once, their loads issued together (each still in s order).
+// Two such sums at once, their loads issued together (each still in s order),
+// kBatch splits of each per round trip.
+template <int kBatch = 8>
 __device__ __forceinline__ void sum_splits_pair(const float4* __restrict__ p, const float4* __restrict__ q,
                                                 size_t stride, int S, float4& a, float4& b) {
     a = b = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < S; s0 += 8) {
-        float4 u[8], v[8];
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+        float4 u[kBatch], v[kBatch];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < kBatch; ++j)
             if (s0 + j < S) {
                 u[j] = __ldg(p + static_cast<size_t>(s0 + j) * stride);
                 v[j] = __ldg(q + static_cast<size_t>(s0 + j) * stride);
             }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kBatch; ++j) {
             if (s0 + j == 0) {
                 a = u[0];
                 b = v[0];
