@@ -112,22 +112,62 @@ def max_over_ranks(v: float, dist) -> float:
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock, power and throttle reasons.
+    """Samples of SM clock, power and clock-event reasons while the bench runs.
 
-    Samples are timestamped on arrival; summary() keeps those that arrived inside
-    the timed windows marked with window()."""
+    A thread reads them through NVML every 5 ms (read-only queries), so that even
+    a 20-call headline window of ~40 ms holds several; without NVML it falls back
+    to nvidia-smi every 200 ms.  Samples are timestamped when taken; summary()
+    keeps those inside the timed windows marked with window()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_S = 0.005
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.samples = []   # (time, sm MHz, max sm MHz, power W, set of reasons)
         self.windows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _nvml_handle(self, nv):
+        try:   # the device torch calls `index`, by its PCI address
+            prop = torch.cuda.get_device_properties(self.index)
+            bus = f"{prop.pci_domain_id:08x}:{prop.pci_bus_id:02x}:{prop.pci_device_id:02x}.0"
+            return nv.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return nv.nvmlDeviceGetHandleByIndex(self.index)
 
     def __enter__(self):
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+            h = self._nvml_handle(nv)
+            bits = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
+                    "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
+                    "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
+                    "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+            smax = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+
+            def poll():
+                while not self._stop.is_set():
+                    try:
+                        sm = float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
+                        pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                        r = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                        self.samples.append((time.monotonic(), sm, smax, pw, {k for k, b in bits.items() if r & b}))
+                    except Exception:
+                        pass
+                    self._stop.wait(self.PERIOD_S)
+
+            self._t = threading.Thread(target=poll, daemon=True)
+            self._t.start()
+            return self
+        except Exception:
+            pass
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -140,49 +180,48 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append((time.monotonic(), line.strip()))
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                reasons = {k for k, f in zip(self.REASONS, parts[4:8]) if f.lower() == "active"}
+                self.samples.append((time.monotonic(), float(parts[0]), float(parts[1]), float(parts[2]), reasons))
+            except ValueError:
+                continue
 
     def wait_first(self, timeout_s: float = 5.0):
         t0 = time.monotonic()
-        while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout_s:
-            time.sleep(0.05)
+        while self._t is not None and not self.samples and time.monotonic() - t0 < timeout_s:
+            time.sleep(0.01)
 
     def window(self, t0: float, t1: float, name: str = "headline"):
         self.windows.append((name, t0, t1))
 
     def __exit__(self, *a):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self._t is not None and self.proc is None:
+            self._t.join(timeout=1.0)
 
     def summary(self, which=("headline",)):
         """Clock record of the samples inside the named timed windows."""
-        sm, smax, power, reasons = [], None, [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         wins = [(a, b) for (n, a, b) in self.windows if n in which]
-        inside = [l for (t, l) in self.lines if any(a <= t <= b + 0.25 for a, b in wins)]
-        for line in inside:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
-                power.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, flag in zip(names, parts[4:8]):
-                if flag.lower() == "active":
-                    reasons.add(name)
+        inside = [smp for smp in list(self.samples) if any(a <= smp[0] <= b for a, b in wins)]
         timed_s = sum(b - a for a, b in wins)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "timed_seconds": round(timed_s, 3), "note": "no nvidia-smi sample inside the timed region"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_median": statistics.median(power) if power else None, "timed_seconds": round(timed_s, 3)}
+        source = "nvml, every 5 ms" if self.proc is None else "nvidia-smi, every 200 ms"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": source,
+                    "timed_seconds": round(timed_s, 3), "note": "no sample inside the timed region"}
+        reasons = set().union(*(smp[4] for smp in inside))
+        return {"sm_mhz": statistics.median(smp[1] for smp in inside), "sm_max_mhz": inside[-1][2],
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_median": statistics.median(smp[3] for smp in inside), "source": source,
+                "timed_seconds": round(timed_s, 3)}
 
 
 # ----------------------------------------------------------------------------- workloads
