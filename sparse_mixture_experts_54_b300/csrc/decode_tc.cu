@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     // ready word (release) after its own wait on the routing kernel.  When the word
     // is set, this kernel reads the schedule at once and its producer sends the
     // first ring's worth of weight tiles before waiting for the SwiGLU kernel; only
-    // the token rows (H) and everything after wait.  The routing kernel of every
+    // the token rows (H) and everything after wait (the MMA and copy-out roles
+    // wait for the SwiGLU kernel as they start).  The routing kernel of every
     // call clears the word once the previous call has finished, so a set word is
     // always this call's.
     bool early = false;
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
+        if (early) griddep_wait();   // only the producer's first weight tiles go ahead of it
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
             int stage = 0;
@@ -287,6 +289,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         __syncwarp();
     } else {
         // ---------------- epilogue: accumulator -> fp32 partial sums ----------------
+        if (early) griddep_wait();
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
