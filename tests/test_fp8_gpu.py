@@ -75,6 +75,7 @@ FP8_CASES = [
     (120, 768, 640, 16, 2),
     (256, 256, 256, 8, 2),
     (16, 256, 256, 8, 8),
+    (24, 6144, 256, 8, 2),      # the longest rows the router's staged W_g allows at 8 experts
 ]
 
 
