@@ -19,6 +19,7 @@ the layer there is) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -114,9 +115,9 @@ def max_over_ranks(v: float, dist) -> float:
 class ClockSampler:
     """Samples of SM clock, power and clock-event reasons while the bench runs.
 
-    A thread reads them through NVML every 5 ms (read-only queries), so that even
-    a 20-call headline window of ~40 ms holds several; without NVML it falls back
-    to nvidia-smi every 200 ms.  Samples are timestamped when taken; summary()
+    A thread reads them through the driver's NVML library every 5 ms (read-only
+    queries, by ctypes), so that even a 20-call headline window of ~40 ms holds
+    several; without it the sampler falls back to nvidia-smi every 200 ms.  Samples are timestamped when taken; summary()
     keeps those inside the timed windows marked with window()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -133,34 +134,54 @@ class ClockSampler:
         self._stop = threading.Event()
         self._t = None
 
-    def _nvml_handle(self, nv):
-        try:   # the device torch calls `index`, by its PCI address
+    @staticmethod
+    def _nvml():
+        """Read-only NVML queries through the driver's library (ctypes): a function
+        returning (sm MHz, power W, clock-event reason bits) and the max SM MHz."""
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit")
+        return lib
+
+    def _nvml_handle(self, lib):
+        h = ctypes.c_void_p()
+        try:   # the device torch calls `index`, found by its PCI address
             prop = torch.cuda.get_device_properties(self.index)
-            bus = f"{prop.pci_domain_id:08x}:{prop.pci_bus_id:02x}:{prop.pci_device_id:02x}.0"
-            return nv.nvmlDeviceGetHandleByPciBusId(bus)
+            bus = f"{prop.pci_domain_id:08x}:{prop.pci_bus_id:02x}:{prop.pci_device_id:02x}.0".encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0:
+                return h
         except Exception:
-            return nv.nvmlDeviceGetHandleByIndex(self.index)
+            pass
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex")
+        return h
 
     def __enter__(self):
         try:
-            import pynvml as nv
-            nv.nvmlInit()
-            h = self._nvml_handle(nv)
-            bits = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
-                    "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
-                    "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
-                    "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
-            smax = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            lib = self._nvml()
+            h = self._nvml_handle(lib)
+            try:
+                get_reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                get_reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            # nvml.h clock-event reason bits
+            bits = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                    "hw_thermal_slowdown": 0x40}
+            NVML_CLOCK_SM = 1
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) != 0:
+                raise RuntimeError("nvmlDeviceGetMaxClockInfo")
+            smax = float(mx.value)
+            clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
 
             def poll():
                 while not self._stop.is_set():
-                    try:
-                        sm = float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
-                        pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
-                        r = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-                        self.samples.append((time.monotonic(), sm, smax, pw, {k for k, b in bits.items() if r & b}))
-                    except Exception:
-                        pass
+                    if (lib.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(clk)) == 0 and
+                            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 and
+                            get_reasons(h, ctypes.byref(rs)) == 0):
+                        r = rs.value
+                        self.samples.append((time.monotonic(), float(clk.value), smax, pw.value / 1000.0,
+                                             {k for k, b in bits.items() if r & b}))
                     self._stop.wait(self.PERIOD_S)
 
             self._t = threading.Thread(target=poll, daemon=True)
