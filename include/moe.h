@@ -81,9 +81,13 @@ typedef enum {
     MOE_OPT_HOST_OUTPUT = 6,   /* moe_forward_host: 1 = when y_host is pinned, the layer's last kernel writes y
                                   into it directly over the bus (default; measured 0.19 ms faster per call at
                                   T=4096), 0 = always copy y back on the stream */
-    MOE_OPT_FP8_WIDEN = 7      /* moe_forward_fp8: 0 = e4m3 weights into the 8-bit MMA against split token rows
+    MOE_OPT_FP8_WIDEN = 7,     /* moe_forward_fp8: 0 = e4m3 weights into the 8-bit MMA against split token rows
                                   (default), 1 = weights widened to bf16 on chip (bitwise equal to the bf16
-                                  path on the dequantised weights; slower) */
+                                  path with MOE_OPT_DECODE_STREAMK 0 on the dequantised weights; slower) */
+    MOE_OPT_DECODE_STREAMK = 8 /* bf16 weight-streaming path, T >= 2: 1 = every CTA streams an equal,
+                                  contiguous share of all touched experts' k-blocks (default), 0 = K split
+                                  uniformly into items (always so at T = 1); the partial sums are grouped
+                                  differently, so results differ in rounding */
 } moe_option_t;
 
 /*

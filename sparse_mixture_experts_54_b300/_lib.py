@@ -33,6 +33,7 @@ MOE_OPT_STAGE_TIMING = 4
 MOE_OPT_GEMM_PAIR = 5
 MOE_OPT_HOST_OUTPUT = 6
 MOE_OPT_FP8_WIDEN = 7
+MOE_OPT_DECODE_STREAMK = 8
 
 # Every entry point declared in include/moe.h, with its ctypes signature.
 _P = ctypes.c_void_p

@@ -45,8 +45,9 @@ struct DecArgs {
     int n;
     int row_blocks;       // weight rows per expert / 128
     int rows_per_e;       // weight rows per expert (F for MODE 0, d for MODE 1)
-    int splits;           // S
-    int kb_per_split;     // K / 64 / S
+    int splits;           // S (uniform splits), 0: stream-K (SplitGeom in kernels.h)
+    int kb_per_split;     // K / 64 / S (uniform)
+    int kb_unit;          // K / 64: k-blocks of a unit
     int n_max;            // largest token count per item, rounded up to 32 (<= 256)
     int stages;
     int stage_bytes;
@@ -158,15 +159,46 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     const int* counts = s_sched;
     const int* offsets = s_sched + n;
     const int n_touched = s_touched[D_MAX_EXPERTS - 1];
-    const int items = n_touched * p.row_blocks * p.splits;
     const KStatus st = p.st;
 
-    // item -> (expert, weight row block, K split); K split varies fastest
-    auto decode_item = [&](int it, int& e, int& rb, int& sp) {
-        sp = it % p.splits;
-        const int r = it / p.splits;
-        rb = r % p.row_blocks;
-        e = s_touched[r / p.row_blocks];
+    // This CTA's work in order: segments (expert, row block, k-blocks [kb0, kb1),
+    // partial-sum slot), by the uniform or the stream-K split (SplitGeom).
+    const int U = n_touched * p.row_blocks;
+    const long long Wk = static_cast<long long>(U) * p.kb_unit;
+    const int Gsk = p.splits == 0 ? sk_grid(Wk, p.kb_unit, gridDim.x) : 0;
+    struct Seg {
+        int e, rb, kb0, kb1, slot;
+    };
+    auto walk_init = [&](long long& cur, long long& end) {
+        if (p.splits == 0) {
+            const bool mine = static_cast<int>(blockIdx.x) < Gsk;
+            cur = mine ? sk_start(blockIdx.x, Wk, Gsk) : 0;
+            end = mine ? sk_start(blockIdx.x + 1, Wk, Gsk) : 0;
+        } else {
+            cur = blockIdx.x;
+            end = static_cast<long long>(U) * p.splits;
+        }
+    };
+    auto walk_next = [&](long long& cur, long long end, Seg& g) -> bool {
+        if (cur >= end) return false;
+        int u;
+        if (p.splits == 0) {
+            u = static_cast<int>(cur / p.kb_unit);
+            g.kb0 = static_cast<int>(cur % p.kb_unit);
+            g.kb1 = static_cast<int>(min(static_cast<long long>(p.kb_unit), g.kb0 + (end - cur)));
+            g.slot = static_cast<int>(blockIdx.x) - sk_cta_of(static_cast<long long>(u) * p.kb_unit, Wk, Gsk);
+            cur += g.kb1 - g.kb0;
+        } else {
+            const int it = static_cast<int>(cur);
+            u = it / p.splits;
+            g.slot = it % p.splits;
+            g.kb0 = g.slot * p.kb_per_split;
+            g.kb1 = g.kb0 + p.kb_per_split;
+            cur += gridDim.x;
+        }
+        g.rb = u % p.row_blocks;
+        g.e = s_touched[u / p.row_blocks];
+        return true;
     };
     auto item_n = [&](int e) {
         const int c = counts[e];
@@ -187,28 +219,28 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             // empty wait) get their byte count and weight tile now; their token
             // rows follow the wait, in the loop below
             int pre = 0;
+            long long cur, end;
+            Seg g;
             if (early) {
-                for (int it = blockIdx.x; it < items && pre < S; it += gridDim.x) {
-                    int e, rb, sp;
-                    decode_item(it, e, rb, sp);
-                    const int nbox = item_n(e) / D_B_BOX;
-                    const int arow = e * p.rows_per_e + rb * 128;
+                walk_init(cur, end);
+                while (pre < S && walk_next(cur, end, g)) {
+                    const int nbox = item_n(g.e) / D_B_BOX;
+                    const int arow = g.e * p.rows_per_e + g.rb * 128;
                     const uint32_t bytes = A_TILES * D_A_BYTES + nbox * D_B_BOX * D_BK * 2;
-                    for (int kb = sp * p.kb_per_split; kb < (sp + 1) * p.kb_per_split && pre < S; ++kb, ++pre) {
+                    for (int kb = g.kb0; kb < g.kb1 && pre < S; ++kb, ++pre) {
                         mbar_arrive_expect_tx(full_bar(pre), bytes);
                         tma_load_2d(ring_u32 + pre * p.stage_bytes, &tmA0, full_bar(pre), kb * D_BK, arow, pol_w);
                     }
                 }
                 griddep_wait();
             }
-            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-                int e, rb, sp;
-                decode_item(it, e, rb, sp);
-                const int nbox = item_n(e) / D_B_BOX;
-                const int arow = e * p.rows_per_e + rb * 128;
-                const int brow = offsets[e];
+            walk_init(cur, end);
+            while (ok && walk_next(cur, end, g)) {
+                const int nbox = item_n(g.e) / D_B_BOX;
+                const int arow = g.e * p.rows_per_e + g.rb * 128;
+                const int brow = offsets[g.e];
                 const uint32_t bytes = A_TILES * D_A_BYTES + nbox * D_B_BOX * D_BK * 2;
-                for (int kb = sp * p.kb_per_split; kb < (sp + 1) * p.kb_per_split; ++kb) {
+                for (int kb = g.kb0; kb < g.kb1; ++kb) {
                     const uint32_t a_dst = ring_u32 + stage * p.stage_bytes;
                     const uint32_t b_dst = a_dst + A_TILES * D_A_BYTES;
                     if (issued >= pre) {
@@ -247,16 +279,17 @@ __global__ void __launch_bounds__(D_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-                int e, rb, sp;
-                decode_item(it, e, rb, sp);
-                const int N = item_n(e);
+            long long cur, end;
+            Seg g;
+            walk_init(cur, end);
+            while (ok && walk_next(cur, end, g)) {
+                const int N = item_n(g.e);
                 const uint32_t idesc = idesc_bf16_f32(128, N);
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, st, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * p.acc_stride);
                 const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
-                for (int k = 0; k < p.kb_per_split; ++k) {
+                for (int k = 0; k < g.kb1 - g.kb0; ++k) {
                     if (!mbar_wait(full_bar(stage), phase, st, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = ring_u32 + stage * p.stage_bytes;
@@ -294,15 +327,17 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < items; it += gridDim.x) {
-            int e, rb, sp;
-            decode_item(it, e, rb, sp);
-            const int N = item_n(e);
-            const int cnt = counts[e];
-            const int off = offsets[e];
+        long long cur, end;
+        Seg g;
+        walk_init(cur, end);
+        while (walk_next(cur, end, g)) {
+            const int N = item_n(g.e);
+            const int cnt = counts[g.e];
+            const int off = offsets[g.e];
+            const int sp = g.slot;
             if (!mbar_wait_warp(accf_bar(acc), acc_phase, st, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const int feat = rb * 128 + q * 32 + lane;   // this thread's weight row = output feature
+            const int feat = g.rb * 128 + q * 32 + lane;   // this thread's weight row = output feature
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
             const uint32_t t0 = tmem_base + static_cast<uint32_t>(acc * p.acc_stride) + lane_off;
             for (int part = 0; part < A_TILES; ++part) {
@@ -341,19 +376,70 @@ __global__ void __launch_bounds__(D_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Per-block view of the split geometry (SplitGeom): how many partial-sum slots
+// the row block rb of expert e has.  Stream-K needs the call's unit count and
+// each expert's rank among the touched ones, from the schedule.
+struct SlotMap {
+    int sk, S, kb, rbe, G;
+    long long W;
+    int rank[D_MAX_EXPERTS];    // touched rank per expert (stream-K)
+    int off[D_MAX_EXPERTS];     // first row per expert
+    int cnt[D_MAX_EXPERTS];     // rows per expert
+    int n;
+};
+
+// Fill (thread 0) a shared SlotMap; the caller synchronises the block after.
+__device__ __forceinline__ void slot_map_init(SlotMap& m, const SplitGeom& g) {
+    m.sk = g.sk;
+    m.S = g.S;
+    m.kb = g.kb;
+    m.rbe = g.rb;
+    m.n = g.n;
+    if (!g.sk) return;
+    int nt = 0;
+    for (int e = 0; e < g.n; ++e) {
+        m.cnt[e] = __ldcg(g.sched + e);
+        m.off[e] = __ldcg(g.sched + g.n + e);
+        m.rank[e] = nt;
+        nt += m.cnt[e] > 0;
+    }
+    m.W = static_cast<long long>(nt) * g.rb * g.kb;
+    m.G = sk_grid(m.W, g.kb, g.grid);
+}
+
+__device__ __forceinline__ int slots_of(const SlotMap& m, int e, int rb) {
+    return m.sk ? sk_slots(m.rank[e] * m.rbe + rb, m.W, m.kb, m.G) : m.S;
+}
+
+// the expert whose rows hold row r (stream-K view; rows are expert-contiguous)
+__device__ __forceinline__ int expert_of_row(const SlotMap& m, int r) {
+    int e_sel = 0;
+    for (int e = 0; e < m.n; ++e)
+        if (m.cnt[e] > 0 && r >= m.off[e]) e_sel = e;
+    return e_sel;
+}
+
 // H[r][f] = bf16( SiLU(sum_s Pa[s][r][f]) * sum_s Pb[s][r][f] ), parts added in order.
-// kBatch: splits per round trip; 2 (S <= 2, the larger batches) leaves registers
-// for 4 blocks per SM, so a T = 32 layer's 896 blocks fit in one wave.
+// kBatch: splits per round trip; 2 (at most 2 slots, the larger batches) leaves
+// registers for 4 blocks per SM, so a T = 32 layer's 896 blocks fit in one wave.
 template <int kBatch>
 __global__ void __launch_bounds__(256, kBatch <= 2 ? 4 : 2)
-    decode_swiglu_kernel(const float4* __restrict__ Pa, const float4* __restrict__ Pb, int S, size_t part4,
-                         uint2* __restrict__ H) {
+    decode_swiglu_kernel(const float4* __restrict__ Pa, const float4* __restrict__ Pb, SplitGeom geo, int F4,
+                         size_t part4, uint2* __restrict__ H) {
+    __shared__ SlotMap sm;
     griddep_launch_dependents();
     griddep_wait();
+    if (threadIdx.x == 0) slot_map_init(sm, geo);
+    __syncthreads();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < part4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        int S = sm.S;
+        if (sm.sk) {
+            const int r = static_cast<int>(i / F4), rb = static_cast<int>(i % F4) / 32;   // 32 float4 = 128 features
+            S = slots_of(sm, expert_of_row(sm, r), rb);
+        }
         float4 a, b;
-        sum_splits_pair<kBatch>(Pa + i, Pb + i, part4, S, a, b);
+        sum_splits_pair<kBatch>(Pa + i, Pb + i, part4, S, S, a, b);
         uint2 o;
         o.x = pack_bf16x2(silu_f(a.x) * b.x, silu_f(a.y) * b.y);
         o.y = pack_bf16x2(silu_f(a.z) * b.z, silu_f(a.w) * b.w);
@@ -366,24 +452,31 @@ __global__ void __launch_bounds__(256, kBatch <= 2 ? 4 : 2)
 // small batches): both slot rows' split loads go out together, one round trip
 // to L2 per 8 splits instead of two; the registers that takes allow one block
 // per SM, which the few blocks of a small batch do not miss.  Same arithmetic
-// in the same order either way.
+// in the same order either way.  Under stream-K a slot row's split count follows
+// its expert (topk_idx) and the row block of the column.
 template <typename TY, bool PAIR>
-__global__ void __launch_bounds__(256, PAIR ? 1 : 2) decode_combine_kernel(const float4* __restrict__ P2, int S, size_t part4,
-                                                             const int32_t* __restrict__ inv,
-                                                             const float* __restrict__ topk_w, int T, int K, int d4,
-                                                             const TY* resid, TY* y) {
+__global__ void __launch_bounds__(256, PAIR ? 1 : 2)
+    decode_combine_kernel(const float4* __restrict__ P2, SplitGeom geo, size_t part4, const int32_t* __restrict__ inv,
+                          const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T, int K, int d4,
+                          const TY* resid, TY* y) {
+    __shared__ SlotMap sm;
     griddep_launch_dependents();
     griddep_wait();
+    if (threadIdx.x == 0) slot_map_init(sm, geo);
+    __syncthreads();
     const size_t total = static_cast<size_t>(T) * d4;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const size_t t = i / d4, c = i % d4;
+        const int rb = static_cast<int>(c) / 32;   // 32 float4 = 128 output features
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (PAIR) {
             const size_t row0 = static_cast<size_t>(inv[2 * t]), row1 = static_cast<size_t>(inv[2 * t + 1]);
             const float g0 = topk_w[2 * t], g1 = topk_w[2 * t + 1];
+            const int S0 = sm.sk ? slots_of(sm, topk_idx[2 * t], rb) : sm.S;
+            const int S1 = sm.sk ? slots_of(sm, topk_idx[2 * t + 1], rb) : sm.S;
             float4 v0, v1;
-            sum_splits_pair(P2 + row0 * d4 + c, P2 + row1 * d4 + c, part4, S, v0, v1);
+            sum_splits_pair(P2 + row0 * d4 + c, P2 + row1 * d4 + c, part4, S0, S1, v0, v1);
             acc.x = fmaf(g0, v0.x, acc.x); acc.y = fmaf(g0, v0.y, acc.y);
             acc.z = fmaf(g0, v0.z, acc.z); acc.w = fmaf(g0, v0.w, acc.w);
             acc.x = fmaf(g1, v1.x, acc.x); acc.y = fmaf(g1, v1.y, acc.y);
@@ -393,6 +486,7 @@ __global__ void __launch_bounds__(256, PAIR ? 1 : 2) decode_combine_kernel(const
                 const size_t a = t * K + k;
                 const size_t row = static_cast<size_t>(inv[a]);
                 const float g = topk_w[a];
+                const int S = sm.sk ? slots_of(sm, topk_idx[a], rb) : sm.S;
                 const float4 v = sum_splits(P2 + row * d4 + c, part4, S);
                 acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
                 acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
@@ -481,7 +575,8 @@ cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3
     args.row_blocks = F / 128;
     args.rows_per_e = F;
     args.splits = splits;
-    args.kb_per_split = d / D_BK / splits;
+    args.kb_unit = d / D_BK;
+    args.kb_per_split = splits > 0 ? d / D_BK / splits : 0;
     args.n_max = (T + D_B_BOX - 1) / D_B_BOX * D_B_BOX;
     args.Pa = Pa;
     args.Pb = Pb;
@@ -502,7 +597,8 @@ cudaError_t launch_decode_w2(const CUtensorMap& mapW2, const CUtensorMap& mapH32
     args.row_blocks = d / 128;
     args.rows_per_e = d;
     args.splits = splits;
-    args.kb_per_split = F / D_BK / splits;
+    args.kb_unit = F / D_BK;
+    args.kb_per_split = splits > 0 ? F / D_BK / splits : 0;
     args.n_max = (T + D_B_BOX - 1) / D_B_BOX * D_B_BOX;
     args.Pa = P2;
     args.Pb = nullptr;
@@ -512,19 +608,34 @@ cudaError_t launch_decode_w2(const CUtensorMap& mapW2, const CUtensorMap& mapH32
     return launch_decode<1>(mapW2, mapW2, mapH32, args, num_sms, s);
 }
 
-cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R, int F, __nv_bfloat16* H,
-                                 cudaStream_t s) {
+SplitGeom decode_geom(int splits, int kblocks, int row_blocks, const int* sched, int n, int num_sms) {
+    SplitGeom g;
+    g.sk = splits == 0;
+    g.S = splits > 0 ? splits : 1;
+    g.kb = kblocks;
+    g.rb = row_blocks;
+    g.grid = num_sms;
+    g.sched = sched;
+    g.n = n;
+    return g;
+}
+
+cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, const SplitGeom& g, int R, int F,
+                                 __nv_bfloat16* H, cudaStream_t s) {
     const size_t part4 = static_cast<size_t>(R) * F / 4;
     int blocks = static_cast<int>((part4 + 255) / 256);
     if (blocks > 148 * 8) blocks = 148 * 8;
     if (blocks < 1) blocks = 1;
-    auto kern = S <= 2 ? decode_swiglu_kernel<2> : decode_swiglu_kernel<8>;
+    // two splits per round trip: uniform S <= 2, or stream-K (W1/W3 rows split in at
+    // most two pieces once the units fill the grid)
+    auto kern = (g.sk || g.S <= 2) ? decode_swiglu_kernel<2> : decode_swiglu_kernel<8>;
     return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(Pa),
-                      reinterpret_cast<const float4*>(Pb), S, part4, reinterpret_cast<uint2*>(H));
+                      reinterpret_cast<const float4*>(Pb), g, F / 4, part4, reinterpret_cast<uint2*>(H));
 }
 
-cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
-                                  int T, int K, int d, const void* resid, void* y, cudaStream_t s) {
+cudaError_t launch_decode_combine(ElemType et, const float* P2, const SplitGeom& g, int R, const int32_t* inv,
+                                  const int32_t* topk_idx, const float* topk_w, int T, int K, int d, const void* resid,
+                                  void* y, cudaStream_t s) {
     const size_t part4 = static_cast<size_t>(R) * d / 4;
     const int d4 = d / 4;
     const size_t total = static_cast<size_t>(T) * d4;
@@ -535,12 +646,13 @@ cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, co
     const bool pair = K == 2 && blocks <= 148;
     if (et == ElemType::BF16) {
         auto kern = pair ? decode_combine_kernel<__nv_bfloat16, true> : decode_combine_kernel<__nv_bfloat16, false>;
-        return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2), S, part4, inv,
-                          topk_w, T, K, d4, static_cast<const __nv_bfloat16*>(resid), static_cast<__nv_bfloat16*>(y));
+        return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2), g, part4, inv,
+                          topk_idx, topk_w, T, K, d4, static_cast<const __nv_bfloat16*>(resid),
+                          static_cast<__nv_bfloat16*>(y));
     }
     auto kern = pair ? decode_combine_kernel<float, true> : decode_combine_kernel<float, false>;
-    return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2), S, part4, inv, topk_w,
-                      T, K, d4, static_cast<const float*>(resid), static_cast<float*>(y));
+    return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(P2), g, part4, inv, topk_idx,
+                      topk_w, T, K, d4, static_cast<const float*>(resid), static_cast<float*>(y));
 }
 
 }  // namespace moe

@@ -131,47 +131,100 @@ __device__ __forceinline__ float4 sum_splits(const float4* __restrict__ p, size_
     return a;
 }
 
-// Two such sums at once, their loads issued together (each still in s order),
-// kBatch splits of each per round trip.
+// Two such sums at once, of S0 and S1 splits, their loads issued together (each
+// still in s order), kBatch splits of each per round trip.
 template <int kBatch = 8>
 __device__ __forceinline__ void sum_splits_pair(const float4* __restrict__ p, const float4* __restrict__ q,
-                                                size_t stride, int S, float4& a, float4& b) {
+                                                size_t stride, int S0, int S1, float4& a, float4& b) {
     a = b = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int S = S0 > S1 ? S0 : S1;
     for (int s0 = 0; s0 < S; s0 += kBatch) {
         float4 u[kBatch], v[kBatch];
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j)
-            if (s0 + j < S) {
-                u[j] = __ldg(p + static_cast<size_t>(s0 + j) * stride);
-                v[j] = __ldg(q + static_cast<size_t>(s0 + j) * stride);
-            }
+        for (int j = 0; j < kBatch; ++j) {
+            if (s0 + j < S0) u[j] = __ldg(p + static_cast<size_t>(s0 + j) * stride);
+            if (s0 + j < S1) v[j] = __ldg(q + static_cast<size_t>(s0 + j) * stride);
+        }
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
             if (s0 + j == 0) {
                 a = u[0];
                 b = v[0];
-            } else if (s0 + j < S) {
-                a.x += u[j].x; a.y += u[j].y; a.z += u[j].z; a.w += u[j].w;
-                b.x += v[j].x; b.y += v[j].y; b.z += v[j].z; b.w += v[j].w;
+            } else {
+                if (s0 + j < S0) {
+                    a.x += u[j].x; a.y += u[j].y; a.z += u[j].z; a.w += u[j].w;
+                }
+                if (s0 + j < S1) {
+                    b.x += v[j].x; b.y += v[j].y; b.z += v[j].z; b.w += v[j].w;
+                }
             }
         }
     }
+}
+
+// How the weight-streaming kernels split K, and so which partial-sum slots the
+// SwiGLU and combine kernels add for a row block.
+//
+// Uniform (sk == 0): item it = (unit, split) with the split fastest; a unit is
+// (touched expert, row block of 128 output features) in expert order; split sp
+// covers k-blocks [sp kb / S, (sp + 1) kb / S) and writes slot sp.
+//
+// Stream-K (sk != 0): the k-blocks of all U units laid end to end, W = U kb, and
+// CTA c of the first G takes [c W / G, (c + 1) W / G) in order, so every CTA
+// streams the same number of weight bytes (to one k-block) and none waits for a
+// last, partly filled wave.  A unit's k-blocks fall to consecutive CTAs; the CTA
+// holding a piece writes slot (its index - the index of the CTA that holds the
+// unit's first k-block), slots 0 .. n_u - 1 in K order.  G is the grid cut so
+// that every CTA's share is at least kb / (kDecodeMaxSplits - 1) k-blocks, hence
+// n_u <= kDecodeMaxSplits.
+struct SplitGeom {
+    int sk = 0;               // 0 uniform, 1 stream-K
+    int S = 1;                // uniform: splits
+    int kb = 1;               // k-blocks per unit
+    int rb = 1;               // row blocks (of 128 output features) per expert
+    int grid = 1;             // CTAs of the weight-streaming launch
+    const int* sched = nullptr;   // stream-K: the call's schedule (counts first)
+    int n = 1;                // experts
+};
+__device__ __forceinline__ long long sk_start(int c, long long W, int G) {
+    return static_cast<long long>(c) * W / G;
+}
+// the CTA whose share holds flat k-block x
+__device__ __forceinline__ int sk_cta_of(long long x, long long W, int G) {
+    return static_cast<int>(((x + 1) * G + W - 1) / W) - 1;
+}
+__device__ __forceinline__ int sk_grid(long long W, int kb, int grid) {
+    const long long m = (kb + kDecodeMaxSplits - 2) / (kDecodeMaxSplits - 1);
+    long long g = W / m;
+    if (g > grid) g = grid;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+// slots holding unit u's partial sums
+__device__ __forceinline__ int sk_slots(int u, long long W, int kb, int G) {
+    return sk_cta_of(static_cast<long long>(u + 1) * kb - 1, W, G) - sk_cta_of(static_cast<long long>(u) * kb, W, G) +
+           1;
 }
 
 int decode_pick_splits(int units, int kblocks, int num_sms);
 // ready (may be null): the schedule-ready word (xchg + kReadyWord) of the
 // routing kernel that ran first in the call; the W1/W3 kernel sets it and the W2
 // kernel then sends its first weight tiles before waiting on the SwiGLU kernel.
+// splits: uniform K splits, or 0 for stream-K.  The SwiGLU and combine
+// launches take the geometry of the launch that wrote their partial sums
+// (decode_geom), and the combine the assignments' experts (topk_idx) to find a
+// row's unit under stream-K.
 cudaError_t launch_decode_w13(const CUtensorMap& mapW1, const CUtensorMap& mapW3, const CUtensorMap& mapXp32,
                               const int* sched, int n, int d, int F, int T, int K, int splits, float* Pa, float* Pb,
                               KStatus st, int num_sms, cudaStream_t s, int* ready = nullptr);
 cudaError_t launch_decode_w2(const CUtensorMap& mapW2_128, const CUtensorMap& mapH32, const int* sched, int n, int d,
                              int F, int T, int K, int splits, float* P2, KStatus st, int num_sms, cudaStream_t s,
                              int* ready = nullptr);
-cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, int S, int R, int F, __nv_bfloat16* H,
+SplitGeom decode_geom(int splits, int kblocks, int row_blocks, const int* sched, int n, int num_sms);
+cudaError_t launch_decode_swiglu(const float* Pa, const float* Pb, const SplitGeom& g, int R, int F, __nv_bfloat16* H,
                                  cudaStream_t s);
-cudaError_t launch_decode_combine(ElemType et, const float* P2, int S, int R, const int32_t* inv, const float* topk_w,
-                                  int T, int K, int d, const void* resid, void* y, cudaStream_t s);
+cudaError_t launch_decode_combine(ElemType et, const float* P2, const SplitGeom& g, int R, const int32_t* inv,
+                                  const int32_t* topk_idx, const float* topk_w, int T, int K, int d, const void* resid,
+                                  void* y, cudaStream_t s);
 
 // the same with e4m3 weights and fp32 row scales (decode_fp8.cu); the weight
 // maps come from encode_map_u8_sw64, the partial sums feed launch_decode_swiglu /

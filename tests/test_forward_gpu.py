@@ -22,12 +22,14 @@ def oracle_y(layer, w, toks, gpu_idx):
     return y, ref, near
 
 
-def run_layer(w, layer, path=0, pair=0):
+def run_layer(w, layer, path=0, pair=0, streamk=1):
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, dtype=w.torch_dtype, bias=layer["bias"])
     if path:
         m.set_option(_lib.MOE_OPT_FORCE_PATH, path)
     if pair:
         m.set_option(_lib.MOE_OPT_GEMM_PAIR, pair)
+    if not streamk:
+        m.set_option(_lib.MOE_OPT_DECODE_STREAMK, 0)
     r = m.route(layer["x"], layer["Wg"])
     y = m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"])
     torch.cuda.synchronize()
@@ -257,10 +259,10 @@ class MixtralCase:
         idx_u, gate_u, _ = reference_selection(dict(logits=logits, idx=idx, gate=gate), gidx, w.k)
         self.y_ref = oracle.moe_tokens(xo, h1, h3, h2, idx_u, gate_u, self.toks)
 
-    def check(self, path=0, pair=0):
+    def check(self, path=0, pair=0, streamk=1):
         w = self.w
         layer = dict(x=self.x, Wg=self.Wg, bias=self.b, W1=self.W1, W3=self.W3, W2=self.W2)
-        m, y, gidx, _ = run_layer(w, layer, path, pair)
+        m, y, gidx, _ = run_layer(w, layer, path, pair, streamk)
         m.close()
         err, bound = assert_close(y_to_numpy(y)[self.toks], self.y_ref, "bf16")
         print(f"{w.name} T={w.T} path={path} pair={pair}: {len(self.toks)} tokens checked {self.info}, "
@@ -315,6 +317,12 @@ def test_mixtral_decode_sweep(decode_cases, T, path):
     decode_cases(T).check(path=path)
 
 
+@pytest.mark.parametrize("T", [8, 32, 128])
+def test_mixtral_decode_uniform_k_split(decode_cases, T):
+    # the weight-streaming kernels with the uniform K split at the Mixtral shape
+    decode_cases(T).check(path=2, streamk=0)
+
+
 # ----------------------------------------------------------------------------- decode (weight-streaming) path
 DECODE_CASES = [
     # T, d, F, n, K
@@ -339,6 +347,28 @@ def test_decode_path_matches_oracle(T, d, F, n, K):
     y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
     check_route(gidx, gw, ref["logits"], ref["idx"], ref["gate"], K)
     assert_close(y_to_numpy(y), y_ref, "bf16")
+
+
+@pytest.mark.parametrize("T,d,F,n,K", DECODE_CASES)
+def test_decode_uniform_k_split_matches_oracle(T, d, F, n, K):
+    # the weight-streaming kernels with K split uniformly into items (the stream-K
+    # split is the default, checked above): same layer, partial sums grouped otherwise
+    w = inputs.Workload("dec", T=T, d=d, d_ff=F, n_experts=n, k=K, seed=100 + T + d)
+    layer = inputs.make_layer(w, "cuda")
+    m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, dtype=w.torch_dtype, bias=layer["bias"])
+    m.set_option(_lib.MOE_OPT_FORCE_PATH, 2)
+    ys = []
+    for sk in (0, 1):
+        m.set_option(_lib.MOE_OPT_DECODE_STREAMK, sk)
+        ys.append(m.forward(layer["x"], layer["Wg"], layer["W1"], layer["W3"], layer["W2"]))
+    torch.cuda.synchronize()
+    assert m.status() == 0, _lib.moe_error_string(m.status())
+    r = m.route(layer["x"], layer["Wg"])
+    gidx = r["topk_idx"].cpu().numpy()
+    y_ref, ref, near = oracle_y(layer, w, np.arange(T), gidx)
+    assert_close(y_to_numpy(ys[0]), y_ref, "bf16")
+    assert_close(y_to_numpy(ys[0]), y_to_numpy(ys[1]), "bf16")
+    m.close()
 
 
 def test_decode_all_tokens_to_one_expert_pair():

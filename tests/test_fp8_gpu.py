@@ -54,6 +54,9 @@ def run_both(w, layer, q, s, widen=1):
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=layer["bias"])
     m.set_option(_lib.MOE_OPT_FORCE_PATH, 2)
     m.set_option(_lib.MOE_OPT_FP8_WIDEN, widen)
+    # the bf16 weight-streaming path with the uniform K split the fp8 kernels use,
+    # so that the widened kernels' partial sums are grouped like its own
+    m.set_option(_lib.MOE_OPT_DECODE_STREAMK, 0)
     r = m.route(layer["x"], layer["Wg"])
     y8 = m.forward_fp8(layer["x"], layer["Wg"], q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     deq = {n: inputs.dequantize_e4m3_rows(q[n], s[n]) for n in NAMES}
@@ -216,8 +219,8 @@ def mixtral_fp8():
 def test_mixtral_decode_fp8(mixtral_fp8, T):
     """Mixtral shape, every token, both kernels against the oracle run on its own
     decoding of the e4m3 bytes; the widening kernel bitwise equal to the bf16
-    weight-streaming path on the dequantised weights, the e4m3 MMA within the
-    bf16 bound of it."""
+    weight-streaming path (uniform K split) on the dequantised weights, the e4m3
+    MMA within the bf16 bound of it."""
     w, q, s, host = mixtral_fp8
     x = inputs.make_x(w, "cuda", seed=None if T == 32 else 60 + T, T=T)
     Wg, b = inputs.make_router(w, "cuda")
@@ -229,6 +232,7 @@ def test_mixtral_decode_fp8(mixtral_fp8, T):
         m.set_option(_lib.MOE_OPT_FP8_WIDEN, widen)
         ys[widen] = m.forward_fp8(x, Wg, q["W1"], s["W1"], q["W3"], s["W3"], q["W2"], s["W2"])
     deq = {n: inputs.dequantize_e4m3_rows(q[n], s[n]) for n in NAMES}
+    m.set_option(_lib.MOE_OPT_DECODE_STREAMK, 0)   # the uniform K split of the fp8 kernels
     y16 = m.forward(x, Wg, deq["W1"], deq["W3"], deq["W2"])
     torch.cuda.synchronize()
     assert m.status() == 0
