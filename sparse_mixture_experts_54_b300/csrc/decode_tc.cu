@@ -380,38 +380,45 @@ __global__ void __launch_bounds__(D_THREADS, 1)
 // the row block rb of expert e has.  Stream-K needs the call's unit count and
 // each expert's rank among the touched ones, from the schedule.
 struct SlotMap {
-    int sk, S, kb, rbe, G;
+    int sk, S, rbe, n, kb, G;
     long long W;
-    int rank[D_MAX_EXPERTS];    // touched rank per expert (stream-K)
+    int rank[D_MAX_EXPERTS];    // touched rank per expert
     int off[D_MAX_EXPERTS];     // first row per expert
     int cnt[D_MAX_EXPERTS];     // rows per expert
-    int n;
 };
 
-// Fill (thread 0) a shared SlotMap; the caller synchronises the block after.
+// All threads of the block; ends with the block synchronised.
 __device__ __forceinline__ void slot_map_init(SlotMap& m, const SplitGeom& g) {
-    m.sk = g.sk;
-    m.S = g.S;
-    m.kb = g.kb;
-    m.rbe = g.rb;
-    m.n = g.n;
-    if (!g.sk) return;
-    int nt = 0;
-    for (int e = 0; e < g.n; ++e) {
-        m.cnt[e] = __ldcg(g.sched + e);
-        m.off[e] = __ldcg(g.sched + g.n + e);
-        m.rank[e] = nt;
-        nt += m.cnt[e] > 0;
+    if (threadIdx.x == 0) {
+        m.sk = g.sk;
+        m.S = g.S;
+        m.rbe = g.rb;
+        m.n = g.n;
+        m.kb = g.kb;
     }
-    m.W = static_cast<long long>(nt) * g.rb * g.kb;
-    m.G = sk_grid(m.W, g.kb, g.grid);
+    if (g.sk && static_cast<int>(threadIdx.x) < g.n) {   // the schedule's words, one per thread
+        m.cnt[threadIdx.x] = __ldcg(g.sched + threadIdx.x);
+        m.off[threadIdx.x] = __ldcg(g.sched + g.n + threadIdx.x);
+    }
+    __syncthreads();
+    if (!g.sk) return;
+    if (threadIdx.x == 0) {
+        int nt = 0;
+        for (int e = 0; e < g.n; ++e) {
+            m.rank[e] = nt;
+            nt += m.cnt[e] > 0;
+        }
+        m.W = static_cast<long long>(nt) * g.rb * g.kb;
+        m.G = sk_grid(m.W, g.kb, g.grid);
+    }
+    __syncthreads();
 }
 
 __device__ __forceinline__ int slots_of(const SlotMap& m, int e, int rb) {
     return m.sk ? sk_slots(m.rank[e] * m.rbe + rb, m.W, m.kb, m.G) : m.S;
 }
 
-// the expert whose rows hold row r (stream-K view; rows are expert-contiguous)
+// the expert whose rows hold row r (rows are expert-contiguous)
 __device__ __forceinline__ int expert_of_row(const SlotMap& m, int r) {
     int e_sel = 0;
     for (int e = 0; e < m.n; ++e)
@@ -429,8 +436,7 @@ __global__ void __launch_bounds__(256, kBatch <= 2 ? 4 : 2)
     __shared__ SlotMap sm;
     griddep_launch_dependents();
     griddep_wait();
-    if (threadIdx.x == 0) slot_map_init(sm, geo);
-    __syncthreads();
+    slot_map_init(sm, geo);
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < part4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         int S = sm.S;
@@ -462,8 +468,7 @@ __global__ void __launch_bounds__(256, PAIR ? 1 : 2)
     __shared__ SlotMap sm;
     griddep_launch_dependents();
     griddep_wait();
-    if (threadIdx.x == 0) slot_map_init(sm, geo);
-    __syncthreads();
+    slot_map_init(sm, geo);
     const size_t total = static_cast<size_t>(T) * d4;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {

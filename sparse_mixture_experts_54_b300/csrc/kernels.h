@@ -189,9 +189,11 @@ struct SplitGeom {
 __device__ __forceinline__ long long sk_start(int c, long long W, int G) {
     return static_cast<long long>(c) * W / G;
 }
-// the CTA whose share holds flat k-block x
+// the CTA whose share holds flat k-block x (32-bit division whenever it fits)
 __device__ __forceinline__ int sk_cta_of(long long x, long long W, int G) {
-    return static_cast<int>(((x + 1) * G + W - 1) / W) - 1;
+    const unsigned long long num = static_cast<unsigned long long>(x + 1) * G + static_cast<unsigned long long>(W) - 1;
+    if (num < (1ull << 32)) return static_cast<int>(static_cast<unsigned>(num) / static_cast<unsigned>(W)) - 1;
+    return static_cast<int>(num / static_cast<unsigned long long>(W)) - 1;
 }
 __device__ __forceinline__ int sk_grid(long long W, int kb, int grid) {
     const long long m = (kb + kDecodeMaxSplits - 2) / (kDecodeMaxSplits - 1);
