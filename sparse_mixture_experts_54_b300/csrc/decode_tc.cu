@@ -9,13 +9,15 @@
 //   MODE 0:  Da = W1_e[rows] . X_e^T,  Db = W3_e[rows] . X_e^T     (128 weight rows x N tokens)
 //   MODE 1:  D  = W2_e[rows] . H_e^T
 //
-// and split K into S parts so that (touched experts) x (row blocks) x S work
-// items spread evenly over all SMs.  Each item writes fp32 partial sums
-// P[s][row of X_e or H_e][output feature]; a small follow-up kernel adds the S
-// parts in order (then SiLU(a)*b for MODE 0, or gate, slot sum and rounding
-// for MODE 1), so results stay bitwise reproducible.
+// and split K so that the work spreads evenly over all SMs: by default every
+// CTA takes an equal, contiguous share of the k-blocks of all (touched expert,
+// row block) units laid end to end (stream-K), else K is cut into S uniform
+// parts per unit (SplitGeom in kernels.h).  Each piece writes fp32 partial sums
+// P[slot][row of X_e or H_e][output feature]; a small follow-up kernel adds a
+// unit's slots in K order (then SiLU(a)*b for MODE 0, or gate, slot sum and
+// rounding for MODE 1), so results stay bitwise reproducible.
 //
-// Pipeline (one CTA per SM, persistent over its items): warp 0 lane 0 streams
+// Pipeline (one CTA per SM, persistent over its pieces): warp 0 lane 0 streams
 // weight tiles (128 rows x 64 K, 128-byte swizzle) and token tiles (32 rows x
 // 64 K) with TMA into a ring of stages sized to the batch; warp 1 owns tensor
 // memory and issues tcgen05.mma (M=128, N = the expert's tokens rounded up to
