@@ -424,7 +424,7 @@ int run_forward_fp8(moe_ctx* c, const void* x, const float* Wg, const uint8_t* W
         CUtensorMap mXq, mHq;
         if (!encode_map_u8_sw128(&mW1, W1q, nF, c->d, 128) || !encode_map_u8_sw128(&mW3, W3q, nF, c->d, 128) ||
             !encode_map_u8_sw128(&mW2, W2q, nd, c->F, 128) ||
-            !encode_map_u8_sw128(&mXq, c->Xq, 2ull * R, c->d, 64) || !encode_map_u8_sw128(&mHq, c->Hq, 2ull * R, c->F, 64))
+            !encode_map_u8_sw128(&mXq, c->Xq, 2ull * R, c->d, 32) || !encode_map_u8_sw128(&mHq, c->Hq, 2ull * R, c->F, 32))
             return MOE_ERR_CUDA;
         const int s0 = decode_pick_splits(touched * (c->F / 128), c->d / 128, c->num_sms);
         s1 = decode_pick_splits(touched * (c->d / 128), c->F / 128, c->num_sms);
