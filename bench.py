@@ -43,7 +43,7 @@ METRIC = "MoE-layer tokens/s (T=4096 prefill) & µs/layer decode T=32; % of BF16
 # define the kernel: the figure is reported only while they are unchanged.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_w13_prefill_t4096.json")
 W13_SOURCES = [os.path.join(ROOT, "sparse_mixture_experts_54_b300", "csrc", f)
-               for f in ("gemm_tc.cu", "common.cuh", "combine_epi.cuh")]
+               for f in ("gemm_tc2.cu", "common.cuh", "combine_epi.cuh")]
 
 
 def w13_source_hash() -> str:
@@ -418,7 +418,7 @@ def run_ours(args, rank, world, dist):
     window_ms = ms_p * args.steps
     kind = "burst" if window_ms <= BURST_WINDOW_MS else "sustained"
     peak = pk["bf16_tflops"] if kind == "burst" else pk["bf16_tflops_sustained"]
-    roofline = {"kernel": "expert_w1w3_swiglu (tcgen05 grouped GEMM + SwiGLU)", "bound": "tensor",
+    roofline = {"kernel": "expert_w1w3_swiglu (tcgen05 grouped GEMM + SwiGLU on CTA pairs)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "peak_kind": f"bf16 {kind} ({pk['source']}): the headline window is {args.steps} calls, "
@@ -764,6 +764,8 @@ def profile_step(args):
     m = MoELayer(w.d, w.d_ff, w.n_experts, w.k, bias=b)
     if args.force_path:
         m.set_option(_lib.MOE_OPT_FORCE_PATH, args.force_path)
+    if args.gemm_pair:
+        m.set_option(_lib.MOE_OPT_GEMM_PAIR, args.gemm_pair)
     if args.fp8:
         q = [inputs.quantize_e4m3_rows(t) for t in (W1, W3, W2)]
         del W1, W3, W2
@@ -797,6 +799,8 @@ def main():
                     help="oracle seconds per reference step (default: min(6, 150 / (warmup + steps)))")
     ap.add_argument("--profile-step", default=None, help="workload name: run warmup+1 untimed calls (for ncu)")
     ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--gemm-pair", type=int, default=0,
+                    help="with --profile-step: grouped-GEMM tiling (1 single CTA, 2 CTA pairs; 0 the default)")
     args = ap.parse_args()
     if args.profile_step:
         profile_step(args)

@@ -74,10 +74,10 @@ typedef enum {
     MOE_OPT_WAIT_LIMIT_US = 2, /* wall-time limit of every bounded wait inside a kernel (default 2,000,000 us) */
     MOE_OPT_FORCE_PATH = 3,    /* 0 = choose by T, 1 = always grouped GEMM, 2 = always decode kernels */
     MOE_OPT_STAGE_TIMING = 4,  /* 1 = record CUDA events around every kernel of moe_forward (see moe_stage_times) */
-    MOE_OPT_GEMM_PAIR = 5,     /* grouped GEMMs: 0 = default (W1/W3 on single CTAs with 128-row tiles, W2 on
-                                  CTA pairs -- tcgen05 cta_group::2, 256/128-row tiles -- when the device can
-                                  co-schedule them), 1 = both single-CTA, 2 = both on CTA pairs or
-                                  MOE_ERR_UNSUPPORTED */
+    MOE_OPT_GEMM_PAIR = 5,     /* grouped GEMMs: 0 = default (both on CTA pairs -- tcgen05 cta_group::2,
+                                  256/128-row tiles -- when the device can co-schedule them, else both on
+                                  single CTAs with 128-row tiles), 1 = both single-CTA, 2 = both on CTA
+                                  pairs or MOE_ERR_UNSUPPORTED */
     MOE_OPT_HOST_OUTPUT = 6,   /* moe_forward_host: 1 = when y_host is pinned, the layer's last kernel writes y
                                   into it directly over the bus (default; measured 0.19 ms faster per call at
                                   T=4096), 0 = always copy y back on the stream */

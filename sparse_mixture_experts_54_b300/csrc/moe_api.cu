@@ -231,11 +231,12 @@ bool use_decode(const moe_ctx* c, int T) {
 }
 
 // Which grouped GEMMs run on CTA pairs.  Pairs move a third fewer operand
-// bytes per FLOP; at the Mixtral shape under the board's power cap that made
-// the W2 GEMM (K = d_ff, long tiles) ~4% faster and the W1/W3 GEMM (K = d)
-// ~4% slower than single CTAs (T = 4096, measured back to back), so by default
-// only W2 runs on pairs.
-bool use_pair13(const moe_ctx* c) { return c->gemm_pair == 2 && pair_gemm_available(c->num_sms); }
+// bytes per FLOP.  At the Mixtral shape, timed in windows of 5-20 calls
+// alternating with single CTAs, a layer with both GEMMs on pairs was 1.5-4.5%
+// faster at T = 4096, ~3% at T = 8192 and ~1.5% on the skewed T = 32768 batch;
+// in 400-call runs at the board's power cap, 1.3% faster.  So by default both
+// run on pairs when the device can co-schedule them (1 forces single CTAs).
+bool use_pair13(const moe_ctx* c) { return c->gemm_pair != 1 && pair_gemm_available(c->num_sms); }
 bool use_pair2(const moe_ctx* c) { return c->gemm_pair != 1 && pair_gemm_available(c->num_sms); }
 
 // Stages of one forward call, in launch order.
