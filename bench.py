@@ -757,7 +757,7 @@ def profile_step(args):
     from sparse_mixture_experts_54_b300.layer import MoELayer
 
     torch.cuda.set_device(0)
-    w = inputs.workload(args.profile_step)
+    w = inputs.workload(args.profile_step, **({"T": args.profile_T} if args.profile_T else {}))
     W1, W3, W2 = inputs.make_experts(w, "cuda")
     x = inputs.make_x(w, "cuda")
     Wg, b = inputs.make_router(w, "cuda")
@@ -776,7 +776,7 @@ def profile_step(args):
             m.forward(x, Wg, W1, W3, W2)
     torch.cuda.synchronize()
     assert m.status() == 0
-    print(f"profile_step {w.name}: {args.warmup + 1} forward calls done", flush=True)
+    print(f"profile_step {w.name} (T={w.T}): {args.warmup + 1} forward calls done", flush=True)
 
 
 def main():
@@ -799,6 +799,7 @@ def main():
                     help="oracle seconds per reference step (default: min(6, 150 / (warmup + steps)))")
     ap.add_argument("--profile-step", default=None, help="workload name: run warmup+1 untimed calls (for ncu)")
     ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--profile-T", type=int, default=0, help="with --profile-step: batch size other than the workload's")
     ap.add_argument("--gemm-pair", type=int, default=0,
                     help="with --profile-step: grouped-GEMM tiling (1 single CTA, 2 CTA pairs; 0 the default)")
     args = ap.parse_args()
