@@ -9,10 +9,11 @@
 //   MODE 0:  Da = W1_e[rows] . X_e^T,  Db = W3_e[rows] . X_e^T     (128 weight rows x N tokens)
 //   MODE 1:  D  = W2_e[rows] . H_e^T
 //
-// and split K so that the work spreads evenly over all SMs: by default every
-// CTA takes an equal, contiguous share of the k-blocks of all (touched expert,
-// row block) units laid end to end (stream-K), else K is cut into S uniform
-// parts per unit (SplitGeom in kernels.h).  Each piece writes fp32 partial sums
+// and split K so that the work spreads evenly over all SMs: by default, from
+// two tokens on, every CTA takes an equal, contiguous share of the k-blocks of
+// all (touched expert, row block) units laid end to end (stream-K); for one
+// token, and when asked, K is cut into S uniform parts per unit (SplitGeom in
+// kernels.h).  Each piece writes fp32 partial sums
 // P[slot][row of X_e or H_e][output feature]; a small follow-up kernel adds a
 // unit's slots in K order (then SiLU(a)*b for MODE 0, or gate, slot sum and
 // rounding for MODE 1), so results stay bitwise reproducible.
